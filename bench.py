@@ -1,0 +1,458 @@
+"""Benchmark of the q3kv verify step (quantise-append + verify attention).
+
+One step = for each of the workload's layers: q3kv_append of every slot's 1+d
+new K/V, then q3kv_verify_attn of the same tokens over the slot's whole cache.
+Default workload: 1 slot, 16 layers, 2 kv / 16 q heads, head_dim 256, 32,768
+cached positions, 6 query tokens (1 + 5 drafts), bf16 inputs.
+
+Prints one JSON line.  ``value`` = verified tokens/s (sum over slots of 1+d per
+step / device time of a step) with the cache and the step's inputs resident on
+the device; ``e2e`` = the same metric through the same C-ABI calls with the
+step's inputs copied from pinned host memory and the outputs copied back inside
+the timed region.  ``roofline`` describes the verify kernel: algorithmic KV
+bytes per launch (224 bytes per attended position per kv head) over its mean
+CUDA-event duration.  ``--impl reference`` times the CPU oracle instead.
+
+Multi-GPU: replicas only (one independent replica per rank, no collective on
+the data path); ``value`` sums all ranks' tokens over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import q3kv_inputs as qi  # noqa: E402
+
+METRIC = "verified tokens/s and KV HBM GB/s (fraction of GB300 peak) for 3-bit verify attn"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 5])
+    ap.add_argument("--verify-impl", default="auto", choices=["auto", "fma", "mma"])
+    ap.add_argument("--split", type=int, default=0, help="positions per split (0 = library policy)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+def dist_init(n):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("gloo")
+        pg = dist
+    return rank, world, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, x):
+    if pg is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for key in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+                if key in d:
+                    v = d[key]
+                    v = v.get("value", v) if isinstance(v, dict) else v
+                    return float(v), "measured"
+        except (ValueError, OSError, TypeError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------------------- our arm
+class Step:
+    """Device buffers and the per-layer append + verify calls of one workload step."""
+
+    def __init__(self, w, verify_impl, split, device):
+        import torch
+
+        from speculative_verify_attention_q3kv_gb300 import api
+
+        self.torch = torch
+        self.api = api
+        self.w = w
+        shapes = qi.draw_shapes(w)
+        self.ctx = shapes.ctx
+        self.n_new = shapes.n_new[0]
+        self.S = w.num_slots
+        self.Ltot = [c + t for c, t in zip(self.ctx, self.n_new)]
+        pages = [(n + 255) // 256 for n in self.Ltot]
+        self.num_pages = sum(pages)
+        self.desc = api.make_desc(w.num_layers, w.num_kv_heads, self.num_pages)
+        self.pool = torch.zeros(api.pool_bytes(self.desc), dtype=torch.uint8, device=device)
+        pt = np.full((self.S, max(pages)), -1, np.int32)
+        k = 0
+        for b, n in enumerate(pages):
+            pt[b, :n] = np.arange(k, k + n)
+            k += n
+        self.page_table = torch.from_numpy(pt).to(device)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.slot_len = torch.tensor(self.ctx, **i32)
+        self.n_new_d = torch.tensor(self.n_new, **i32)
+        offs = np.concatenate([[0], np.cumsum(self.n_new)]).astype(np.int32)
+        self.row_off = torch.from_numpy(offs).to(device)
+        self.ctx_len = torch.tensor(self.Ltot, **i32)
+        self.rows = int(offs[-1])
+        self.max_new = max(self.n_new)
+        self.max_ctx = max(self.Ltot)
+        self.dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+        self.impl = {"auto": 0, "fma": 1, "mma": 2}[verify_impl]
+        self.split = split
+        self.ws = torch.zeros(api.workspace_bytes(self.desc, self.S, self.max_ctx, self.max_new, self.impl, split),
+                              dtype=torch.uint8, device=device)
+        self.status = torch.zeros(1, **i32)
+        self.device = device
+        H, Hq, D, Ly = w.num_kv_heads, w.num_q_heads, w.head_dim, w.num_layers
+        g = torch.Generator(device=device)
+        g.manual_seed(1000 + w.seed)
+        # step inputs: new K, V [layers, rows, H, D]; Q [layers, rows, Hq, D]
+        self.k_new = torch.empty((Ly, self.rows, H, D), dtype=self.dt, device=device)
+        self.v_new = torch.empty_like(self.k_new)
+        self.q = (torch.randn((Ly, self.rows, Hq, D), generator=g, device=device)).to(self.dt)
+        for l in range(Ly):
+            for h in range(H):
+                qi.torch_fill_kv_(self.k_new[l, :, h], w, l, h, 0, g)
+                qi.torch_fill_kv_(self.v_new[l, :, h], w, l, h, 1, g)
+        self.out = torch.empty((Ly, self.rows, Hq, D), dtype=torch.float32, device=device)
+        self._prefill(g)
+
+    def _prefill(self, g):
+        torch, api, w = self.torch, self.api, self.w
+        chunk = 32768
+        zero = torch.zeros(self.S, dtype=torch.int32, device=self.device)
+        for l in range(w.num_layers):
+            for b in range(self.S):
+                for start in range(0, self.ctx[b], chunk):
+                    n = min(chunk, self.ctx[b] - start)
+                    kk = torch.empty((n, w.num_kv_heads, w.head_dim), dtype=self.dt, device=self.device)
+                    vv = torch.empty_like(kk)
+                    for h in range(w.num_kv_heads):
+                        qi.torch_fill_kv_(kk[:, h], w, l, h, 0, g)
+                        qi.torch_fill_kv_(vv[:, h], w, l, h, 1, g)
+                    lens = zero.clone()
+                    lens[b] = start
+                    nn = zero.clone()
+                    nn[b] = n
+                    offs = torch.zeros(self.S + 1, dtype=torch.int32, device=self.device)
+                    offs[b + 1:] = n
+                    api.append(self.desc, self.pool, self.page_table, lens, nn, offs, n, l, kk, vv, self.status)
+        torch.cuda.synchronize()
+        assert int(self.status.item()) == 0, "prefill flagged a device status"
+
+    def kv_bytes_per_layer(self):
+        return sum(self.Ltot) * self.w.num_kv_heads * 224
+
+    def run(self, verify_events=None, k_new=None, v_new=None, q=None, out=None):
+        api = self.api
+        k_new = self.k_new if k_new is None else k_new
+        v_new = self.v_new if v_new is None else v_new
+        q = self.q if q is None else q
+        out = self.out if out is None else out
+        for l in range(self.w.num_layers):
+            api.append(self.desc, self.pool, self.page_table, self.slot_len, self.n_new_d, self.row_off,
+                       self.max_new, l, k_new[l], v_new[l], self.status)
+            if verify_events is not None:
+                verify_events[l][0].record()
+            api.verify_attn(self.desc, self.pool, self.page_table, self.ctx_len, self.n_new_d, self.row_off,
+                            self.max_ctx, self.max_new, l, q[l], out[l], self.ws, self.impl, self.split, self.status)
+            if verify_events is not None:
+                verify_events[l][1].record()
+
+
+def run_ours(args, rank, world, local, pg):
+    import torch
+
+    from speculative_verify_attention_q3kv_gb300 import build as b
+
+    b.build()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    w = qi.WORKLOADS[args.workload]
+    st = Step(w, args.verify_impl, args.split, device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    tokens_per_step = sum(st.n_new)
+    Ly = w.num_layers
+
+    for _ in range(max(args.warmup, 3)):
+        st.run()
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    vev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ly)]
+           for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(pg)
+    torch.cuda.synchronize()
+    clocks.start()
+    for s in range(args.steps):
+        flush.zero_()                       # L2 flush between timed steps (outside the events)
+        ev[s][0].record(stream)
+        st.run(verify_events=vev[s])
+        ev[s][1].record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    barrier(pg)
+    step_ms = [a.elapsed_time(b_) for a, b_ in ev]
+    verify_ms = [a.elapsed_time(b_) for row in vev for a, b_ in row]
+    total_s = max_over_ranks(pg, sum(step_ms) / 1e3)
+    assert int(st.status.item()) == 0, "device status flagged during the benchmark"
+
+    # ---- end to end: inputs from pinned host memory, outputs back to host, inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hk = st.k_new.cpu().pin_memory()
+        hv = st.v_new.cpu().pin_memory()
+        hq = st.q.cpu().pin_memory()
+        ho = torch.empty(st.out.shape, dtype=torch.float32).pin_memory()
+        dk, dv, dq, do = (torch.empty_like(st.k_new), torch.empty_like(st.v_new), torch.empty_like(st.q),
+                          torch.empty_like(st.out))
+        e_ms = []
+        for s in range(max(args.warmup, 3) + args.steps):
+            flush.zero_()
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            dq.copy_(hq, non_blocking=True)
+            st.run(k_new=dk, v_new=dv, q=dq, out=do)
+            ho.copy_(do, non_blocking=True)
+            b_.record(stream)
+            torch.cuda.synchronize()
+            if s >= max(args.warmup, 3):
+                e_ms.append(a.elapsed_time(b_))
+        e2e_s = max_over_ranks(pg, sum(e_ms) / 1e3)
+        h2d = hk.numel() * hk.element_size() + hv.numel() * hv.element_size() + hq.numel() * hq.element_size()
+        d2h = ho.numel() * ho.element_size()
+        e2e = {"value": world * tokens_per_step * args.steps / e2e_s, "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peak_hbm()
+    mean_verify_s = statistics.mean(verify_ms) / 1e3
+    kv_bytes = st.kv_bytes_per_layer()
+    achieved = kv_bytes / mean_verify_s / 1e9
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(w, budget_s=20.0)
+    line = {
+        "metric": METRIC,
+        "value": world * tokens_per_step * args.steps / total_s,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": total_s * 1e3 / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded; K,V per-channel 10^U(0,1) outliers, Q N(0,1))" if w.kv_dist == "loguniform10"
+                else "synthetic (seeded; K,V N(0,1) with 4 outlier channels x8)",
+        "config": {"workload": w.name, "slots": w.num_slots, "layers": Ly, "kv_heads": w.num_kv_heads,
+                   "q_heads": w.num_q_heads, "head_dim": w.head_dim, "ctx": st.ctx, "query_tokens": st.n_new,
+                   "page_size": 256, "verify_impl": args.verify_impl, "split_positions": args.split,
+                   "l2": "flushed between timed steps (256 MiB write)", "parallelism": f"replicas{world}"},
+        "kv_gbs": kv_bytes * Ly * args.steps / (sum(verify_ms) / 1e3) / 1e9,
+        "verify_only_tokens_per_s": tokens_per_step * args.steps / (sum(verify_ms) / 1e3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "q3kv verify (one launch per layer)", "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": kv_bytes,
+                     "mean_launch_us": mean_verify_s * 1e6},
+        "clocks": clock_info,
+        "gpu_launches": args.steps * Ly * 2,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) arm
+_PREFILLED = {}
+
+
+def _oracle_layer_sample(w, layer, shapes):
+    """Run the oracle's append + verify for one layer of every slot; returns (tokens, seconds of the step part)."""
+    from oracle.cache import PagedCache
+
+    S = w.num_slots
+    Ltot = [c + t for c, t in zip(shapes.ctx, shapes.n_new[0])]
+    pages = [(n + 255) // 256 for n in Ltot]
+    pt = np.full((S, max(pages)), -1, np.int32)
+    k = 0
+    for b, n in enumerate(pages):
+        pt[b, :n] = np.arange(k, k + n)
+        k += n
+    if (w.key, layer) not in _PREFILLED:
+        cache = PagedCache(sum(pages), 1, w.num_kv_heads)
+        for b in range(S):                             # prefill (set-up, not timed)
+            kk = np.stack([qi.kv_rows(w, b, layer, g, 0, 0, shapes.ctx[b]) for g in range(w.num_kv_heads)], axis=1)
+            vv = np.stack([qi.kv_rows(w, b, layer, g, 1, 0, shapes.ctx[b]) for g in range(w.num_kv_heads)], axis=1)
+            cache.append(pt[b], 0, 0, kk, vv)
+        _PREFILLED[(w.key, layer)] = cache
+    cache = _PREFILLED[(w.key, layer)]
+    t0 = time.perf_counter()
+    for b in range(S):                                 # the step: append the new tokens, verify them
+        n, T = shapes.ctx[b], shapes.n_new[0][b]
+        kk = np.stack([qi.kv_rows(w, b, layer, g, 0, n, T) for g in range(w.num_kv_heads)], axis=1)
+        vv = np.stack([qi.kv_rows(w, b, layer, g, 1, n, T) for g in range(w.num_kv_heads)], axis=1)
+        cache.append(pt[b], n, 0, kk, vv)
+        cache.verify(pt[b], 0, n, qi.q_rows(w, b, layer, 0, T), w.group)
+    return sum(shapes.n_new[0]), time.perf_counter() - t0
+
+
+def cpu_baseline(w, budget_s=20.0):
+    shapes = qi.draw_shapes(w)
+    spent, layers = 0.0, 0
+    while spent < budget_s and layers < w.num_layers:
+        _, dt = _oracle_layer_sample(w, layers, shapes)
+        spent += dt
+        layers += 1
+    per_layer = spent / layers
+    tokens = sum(shapes.n_new[0])
+    return {"value": tokens / (per_layer * w.num_layers), "unit": "tokens/s", "cores": _threads(),
+            "kind": "oracle",
+            "sample": f"{layers} of {w.num_layers} layers of one step (append + verify, every slot), "
+                      f"scaled to {w.num_layers} layers; prefill not timed"}
+
+
+def _threads():
+    try:
+        import threadpoolctl
+
+        n = max((p.get("num_threads", 1) for p in threadpoolctl.threadpool_info()), default=1)
+        return int(n)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = qi.WORKLOADS[args.workload]
+    shapes = qi.draw_shapes(w)
+    times = []
+    for s in range(max(args.warmup, 3) + args.steps):
+        tok, dt = _oracle_layer_sample(w, s % w.num_layers, shapes)
+        if s >= max(args.warmup, 3):
+            times.append(dt * w.num_layers)           # one sampled layer stands for all layers
+    total = sum(times)
+    value = tok * args.steps / total
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": total * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "slots": w.num_slots, "layers": w.num_layers, "ctx": shapes.ctx,
+                       "query_tokens": shapes.n_new[0]},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _threads(), "kind": "oracle",
+                             "sample": "each step runs one layer of the step (append + verify of every slot) "
+                                       "and counts it for all layers"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local, pg = dist_init(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local, pg)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

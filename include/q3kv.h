@@ -1,0 +1,185 @@
+/*
+ * q3kv -- speculative-verify attention over a 3-bit, Walsh-Hadamard-rotated,
+ * paged KV cache.  C ABI of the shared library libq3kv.so (sm_103a).
+ *
+ * Source of the method: the "Quasar" (q27) engine wiki --
+ *   - "turbo3 3-bit KV cache" bullet and the "KV cache" stack bullet: K and V
+ *     are WHT-rotated and stored as 3-bit codes in fixed-size blocks,
+ *     symmetric for K and V, per slot;
+ *   - "Self-speculation as the whole design": all drafted tokens of a step are
+ *     checked in one shared-KV verify pass;
+ *   - "Width-12 verify": up to 12 tokens per step (this library takes up to 16);
+ *   - "Continuous batching": several slots go through one fused round.
+ * The pages give no bit-level codec and no kernel for this GPU.  The codec
+ * here is this library's own (head_dim 256; y = H x in float32 with H the
+ * orthonormal Sylvester-Hadamard matrix; 8 blocks of 32; per block an fp16
+ * scale s = absmax/3.5 and codes q = clamp(rint(y/s + 3.5), 0, 7); value
+ * (q - 3.5) s; 112 bytes per vector).  Queries are rotated by the same H; the
+ * output is rotated back, so callers see ordinary attention outputs.
+ *
+ * Conventions for every call:
+ *   - Return value: Q3KV_OK (0) or a negative Q3KV_ERR_* code.  Nothing is
+ *     launched when an argument check fails.
+ *   - Device-side problems (a page id outside [0, num_pages), a length beyond
+ *     the slot's page table, a non-finite input, an fp16 scale overflow) never
+ *     trap: the kernel ORs a Q3KV_STATUS_* bit into *d_status and skips the
+ *     offending unit.  d_status may be NULL to ignore them.
+ *   - All device work is asynchronous on the given stream.  Pointers prefixed
+ *     d_ are device pointers; h_ are host pointers.  The library allocates no
+ *     device memory: the caller owns the pool, page tables, lengths, inputs,
+ *     outputs, workspace and status word.
+ *   - Lengths are owned by the caller.  Rolling back rejected drafts is a
+ *     smaller length on the next call; stale records are overwritten by the
+ *     next append.
+ */
+#ifndef Q3KV_H
+#define Q3KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define Q3KV_API __attribute__((visibility("default")))
+#else
+#define Q3KV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define Q3KV_FORMAT_VERSION 1   /* bumps when the record or page layout changes */
+
+/* error codes (return values) */
+#define Q3KV_OK                      0
+#define Q3KV_ERR_INVALID_ARG        -1
+#define Q3KV_ERR_UNSUPPORTED        -2
+#define Q3KV_ERR_OUT_OF_PAGES       -3
+#define Q3KV_ERR_WORKSPACE_TOO_SMALL -4
+#define Q3KV_ERR_CUDA               -5
+#define Q3KV_ERR_SLOT_RANGE         -6
+
+/* device status bits (*d_status) */
+#define Q3KV_STATUS_NONFINITE_INPUT  1
+#define Q3KV_STATUS_SCALE_OVERFLOW   2
+#define Q3KV_STATUS_BAD_PAGE         4
+#define Q3KV_STATUS_BAD_LENGTH       8
+
+/* input dtypes */
+#define Q3KV_F32   0
+#define Q3KV_BF16  1
+
+/* verify implementations */
+#define Q3KV_IMPL_AUTO  0   /* the fastest one that supports the shape          */
+#define Q3KV_IMPL_FMA   1   /* CUDA-core fp32 FMA flash-decode (reference leg)   */
+#define Q3KV_IMPL_MMA   2   /* tensor-core leg                                  */
+
+/* Shape of one cache pool.  Supported: head_dim 256, page_size 256,
+ * num_q_heads = 8 * num_kv_heads (GQA group of 8), num_kv_heads >= 1. */
+typedef struct q3kv_cache_desc {
+    int32_t num_layers;
+    int32_t num_kv_heads;
+    int32_t num_q_heads;
+    int32_t head_dim;    /* 256 */
+    int32_t page_size;   /* 256 */
+    int32_t num_pages;
+} q3kv_cache_desc;
+
+/* Library and layout versions. */
+Q3KV_API int q3kv_version(void);
+Q3KV_API int q3kv_format_version(void);
+
+/* Text of an error code (static string, never NULL). */
+Q3KV_API const char* q3kv_strerror(int err);
+
+/* Bytes of a pool for desc:
+ *   num_pages * num_layers * num_kv_heads * 2 * page_size * 112.
+ * Pool layout: the 112-byte record of (page, layer, kv_head, kv in {0:K, 1:V},
+ * row = position % 256) starts at
+ *   ((((page*num_layers + layer)*num_kv_heads + kv_head)*2 + kv)*256 + row)*112.
+ * Record: 24 little-endian uint32 code words (three per 32-element block; in
+ * block b, element e < 30 is pair m = e/2, half = e%2, in word 3b + m/5 at bit
+ * 16*half + 3*(m%5); element 30 keeps code bit k in bit 15 of word 3b+k and
+ * element 31 in bit 31), then 8 fp16 scales.  The pool must be 16-byte aligned. */
+Q3KV_API int q3kv_pool_bytes(const q3kv_cache_desc* desc, size_t* bytes);
+
+/* ---- host page allocator (no device work) --------------------------------
+ * Source: per-slot KV of the "turbo3 3-bit KV cache" bullet, and the
+ * PagedAttention paragraph of the prefix-reuse section (a pool of fixed-size
+ * blocks).  Pages are 256 positions.  The allocator owns only host state. */
+typedef struct q3kv_allocator q3kv_allocator;
+
+/* Create an allocator over page ids [0, num_pages) for num_slots slots whose
+ * page-table rows hold max_pages_per_slot entries.  *out receives the handle. */
+Q3KV_API int q3kv_allocator_create(int32_t num_pages, int32_t num_slots, int32_t max_pages_per_slot,
+                          q3kv_allocator** out);
+Q3KV_API void q3kv_allocator_destroy(q3kv_allocator* a);
+
+/* Make slot hold pages for n_positions positions (ceil(n/256) pages), taking
+ * new pages from the free list.  Writes the slot's page ids into the caller's
+ * host row h_page_table_row[0 .. *n_pages_out) (length max_pages_per_slot;
+ * entries past the count are set to -1).  Never shrinks.  All or nothing: on
+ * Q3KV_ERR_OUT_OF_PAGES nothing changes. */
+Q3KV_API int q3kv_alloc_pages(q3kv_allocator* a, int32_t slot, int64_t n_positions,
+                     int32_t* h_page_table_row, int32_t* n_pages_out);
+
+/* Return all pages of slot to the free list. */
+Q3KV_API int q3kv_free_slot(q3kv_allocator* a, int32_t slot);
+
+/* Free pages left. */
+Q3KV_API int q3kv_free_pages(const q3kv_allocator* a, int32_t* n_free);
+
+/* ---- quantise-append --------------------------------------------------------
+ * Encodes new raw K and V head vectors and writes their records.  Slot b
+ * appends d_n_new[b] tokens at positions [d_slot_len[b], d_slot_len[b] +
+ * d_n_new[b]); token t of slot b is input row d_row_offsets[b] + t.
+ *   k, v           device, [rows, num_kv_heads, 256], dtype f32 or bf16,
+ *                  unrotated; rows = d_row_offsets[num_slots]
+ *   d_page_table   device int32 [num_slots, max_pages_per_slot]
+ *   d_slot_len     device int32 [num_slots], positions before the append
+ *   d_n_new        device int32 [num_slots], 0 allowed
+ *   d_row_offsets  device int32 [num_slots + 1]
+ *   max_n_new      host bound on d_n_new[b] (sizes the launch; larger device
+ *                  values set Q3KV_STATUS_BAD_LENGTH and are skipped)
+ * A record whose page id is out of range is skipped with Q3KV_STATUS_BAD_PAGE. */
+Q3KV_API int q3kv_append(void* stream, const q3kv_cache_desc* desc, void* d_pool,
+                const int32_t* d_page_table, int32_t max_pages_per_slot,
+                const int32_t* d_slot_len, const int32_t* d_n_new, const int32_t* d_row_offsets,
+                int32_t num_slots, int32_t max_n_new, int32_t layer,
+                const void* k, const void* v, int32_t dtype, int32_t* d_status);
+
+/* ---- verify attention ------------------------------------------------------
+ * For slot b with L_b = d_ctx_len[b] positions already in the cache (the new
+ * tokens appended) and T_b = d_n_q[b] query tokens, query token t in [0, T_b)
+ * of q head h attends to positions [0, L_b - T_b + t] of kv head h / 8:
+ *   out = H softmax((H q) . k_hat / 16) v_hat        (float32 output)
+ *   q      device [rows, num_q_heads, 256], f32 or bf16, unrotated;
+ *          token t of slot b is row d_q_offsets[b] + t
+ *   out    device float32, same indexing as q
+ *   max_ctx_len, max_n_q   host bounds of d_ctx_len and d_n_q (size the
+ *          launch); max_n_q <= 16
+ *   impl   Q3KV_IMPL_*;  split_positions: positions per split-K unit
+ *          (multiple of 256; 0 = chosen from the shape and the GPU)
+ *   workspace, workspace_bytes: device scratch of at least
+ *          q3kv_workspace_bytes(...) bytes for the same arguments; it must be
+ *          zero-filled once before first use (the kernels leave their merge
+ *          counters at zero again when they finish).  Calls that share one
+ *          workspace must not overlap on the GPU.
+ * Slots with T_b == 0 produce nothing.  T_b > L_b or L_b beyond the slot's
+ * page table sets Q3KV_STATUS_BAD_LENGTH and the slot's rows are left as they
+ * were. */
+Q3KV_API int q3kv_workspace_bytes(const q3kv_cache_desc* desc, int32_t num_slots, int64_t max_ctx_len,
+                         int32_t max_n_q, int32_t impl, int32_t split_positions, size_t* bytes);
+
+Q3KV_API int q3kv_verify_attn(void* stream, const q3kv_cache_desc* desc, const void* d_pool,
+                     const int32_t* d_page_table, int32_t max_pages_per_slot,
+                     const int32_t* d_ctx_len, const int32_t* d_n_q, const int32_t* d_q_offsets,
+                     int32_t num_slots, int64_t max_ctx_len, int32_t max_n_q, int32_t layer,
+                     const void* q, int32_t dtype, float* out,
+                     int32_t impl, int32_t split_positions,
+                     void* d_workspace, size_t workspace_bytes, int32_t* d_status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* Q3KV_H */

@@ -1,0 +1,128 @@
+"""Thin Python layer over the C ABI: torch tensors in, raw pointers out.
+
+Argument marshalling only -- every step of the hot path runs in the CUDA
+library.  Names follow ``include/q3kv.h``.  Device buffers are torch tensors the
+caller owns; the library never allocates device memory.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import CacheDesc, Q3KVError, check  # noqa: F401  (re-exported)
+
+HEAD_DIM = 256
+PAGE_SIZE = 256
+GROUP = 8
+
+
+def make_desc(num_layers: int, num_kv_heads: int, num_pages: int) -> CacheDesc:
+    return CacheDesc(num_layers, num_kv_heads, GROUP * num_kv_heads, HEAD_DIM, PAGE_SIZE, num_pages)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to q3kv must be contiguous")
+    return t.data_ptr()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return _lib.Q3KV_F32
+    if t.dtype == torch.bfloat16:
+        return _lib.Q3KV_BF16
+    raise TypeError(f"q3kv inputs must be float32 or bfloat16, got {t.dtype}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def pool_bytes(desc: CacheDesc) -> int:
+    n = ctypes.c_size_t()
+    check(_lib.load().q3kv_pool_bytes(ctypes.byref(desc), ctypes.byref(n)), "q3kv_pool_bytes")
+    return n.value
+
+
+def workspace_bytes(desc: CacheDesc, num_slots: int, max_ctx_len: int, max_n_q: int,
+                    impl: int = _lib.Q3KV_IMPL_AUTO, split_positions: int = 0) -> int:
+    n = ctypes.c_size_t()
+    check(_lib.load().q3kv_workspace_bytes(ctypes.byref(desc), num_slots, max_ctx_len, max_n_q, impl,
+                                           split_positions, ctypes.byref(n)), "q3kv_workspace_bytes")
+    return n.value
+
+
+class Allocator:
+    """Host free-list page allocator (q3kv_allocator_*)."""
+
+    def __init__(self, num_pages: int, num_slots: int, max_pages_per_slot: int):
+        self._lib = _lib.load()
+        h = ctypes.c_void_p()
+        check(self._lib.q3kv_allocator_create(num_pages, num_slots, max_pages_per_slot, ctypes.byref(h)),
+              "q3kv_allocator_create")
+        self._h = h
+        self.max_pages_per_slot = max_pages_per_slot
+
+    def alloc_pages(self, slot: int, n_positions: int) -> np.ndarray:
+        row = np.full(self.max_pages_per_slot, -1, dtype=np.int32)
+        n = ctypes.c_int32()
+        check(self._lib.q3kv_alloc_pages(self._h, slot, n_positions,
+                                         row.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), ctypes.byref(n)),
+              "q3kv_alloc_pages")
+        return row
+
+    def free_slot(self, slot: int) -> None:
+        check(self._lib.q3kv_free_slot(self._h, slot), "q3kv_free_slot")
+
+    def free_pages(self) -> int:
+        n = ctypes.c_int32()
+        check(self._lib.q3kv_free_pages(self._h, ctypes.byref(n)), "q3kv_free_pages")
+        return n.value
+
+    def close(self) -> None:
+        if self._h:
+            self._lib.q3kv_allocator_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def append(desc: CacheDesc, pool: torch.Tensor, page_table: torch.Tensor, slot_len: torch.Tensor,
+           n_new: torch.Tensor, row_offsets: torch.Tensor, max_n_new: int, layer: int,
+           k: torch.Tensor, v: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """q3kv_append: quantise and store k, v [rows, kv_heads, 256] for each slot."""
+    if k.dtype != v.dtype:
+        raise TypeError("k and v must share a dtype")
+    rc = _lib.load().q3kv_append(_stream(stream), ctypes.byref(desc), _ptr(pool), _ptr(page_table),
+                                 page_table.shape[1], _ptr(slot_len), _ptr(n_new), _ptr(row_offsets),
+                                 slot_len.shape[0], max_n_new, layer, _ptr(k), _ptr(v), _dtype_code(k),
+                                 _ptr(status))
+    check(rc, "q3kv_append")
+
+
+def verify_attn(desc: CacheDesc, pool: torch.Tensor, page_table: torch.Tensor, ctx_len: torch.Tensor,
+                n_q: torch.Tensor, q_offsets: torch.Tensor, max_ctx_len: int, max_n_q: int, layer: int,
+                q: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
+                impl: int = _lib.Q3KV_IMPL_AUTO, split_positions: int = 0,
+                status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """q3kv_verify_attn: out[rows, q_heads, 256] (float32) for every slot's query tokens."""
+    if out.dtype != torch.float32:
+        raise TypeError("out must be float32")
+    rc = _lib.load().q3kv_verify_attn(_stream(stream), ctypes.byref(desc), _ptr(pool), _ptr(page_table),
+                                      page_table.shape[1], _ptr(ctx_len), _ptr(n_q), _ptr(q_offsets),
+                                      ctx_len.shape[0], max_ctx_len, max_n_q, layer, _ptr(q), _dtype_code(q),
+                                      _ptr(out), impl, split_positions, _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _ptr(status))
+    check(rc, "q3kv_verify_attn")

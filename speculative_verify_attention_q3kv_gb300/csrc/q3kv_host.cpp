@@ -1,0 +1,266 @@
+// Host side of the C ABI: argument checks, the page allocator, workspace
+// sizing, split-K policy and kernel dispatch.  No device memory is allocated
+// here; every device buffer belongs to the caller.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "q3kv_internal.h"
+
+using namespace q3kv;
+
+namespace {
+
+constexpr int kVersion = 1;
+
+int check_desc(const q3kv_cache_desc* d) {
+    if (!d) return Q3KV_ERR_INVALID_ARG;
+    if (d->num_layers <= 0 || d->num_kv_heads <= 0 || d->num_pages <= 0 || d->num_q_heads <= 0)
+        return Q3KV_ERR_INVALID_ARG;
+    if (d->head_dim != kHeadDim || d->page_size != kPageSize) return Q3KV_ERR_UNSUPPORTED;
+    if (d->num_q_heads != kGroup * d->num_kv_heads) return Q3KV_ERR_UNSUPPORTED;
+    if (d->num_kv_heads > 64) return Q3KV_ERR_UNSUPPORTED;
+    return Q3KV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int device_sm_count(int* sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return Q3KV_ERR_CUDA;
+    if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return Q3KV_ERR_CUDA;
+    return Q3KV_OK;
+}
+
+struct Plan {
+    int impl;
+    int rows_per_chunk;
+    int row_chunks;
+    int split_pages;
+    int num_splits;
+    size_t part_o_bytes;
+    size_t part_ml_bytes;
+    size_t ticket_bytes;
+    size_t total() const { return part_o_bytes + part_ml_bytes + ticket_bytes; }
+};
+
+// Split-K policy: enough (slot, kv head, row chunk, split) CTAs to cover the
+// GPU about twice over, splits a whole number of pages.
+int make_plan(const q3kv_cache_desc* d, int32_t num_slots, int64_t max_ctx, int32_t max_n_q, int32_t impl,
+              int32_t split_positions, Plan* p) {
+    if (num_slots < 0 || max_ctx < 0 || max_n_q < 0 || max_n_q > kMaxNq) return Q3KV_ERR_INVALID_ARG;
+    if (split_positions < 0 || split_positions % kPageSize != 0) return Q3KV_ERR_INVALID_ARG;
+    if (max_ctx > (int64_t)INT32_MAX - kPageSize) return Q3KV_ERR_INVALID_ARG;
+    if (impl == Q3KV_IMPL_AUTO) impl = Q3KV_IMPL_FMA;
+    if (impl != Q3KV_IMPL_FMA) return Q3KV_ERR_UNSUPPORTED;
+    p->impl = impl;
+    p->rows_per_chunk = kFmaRows;
+    const int rows = kGroup * std::max<int32_t>(max_n_q, 1);
+    p->row_chunks = (rows + p->rows_per_chunk - 1) / p->rows_per_chunk;
+    const int64_t pages = std::max<int64_t>(1, (max_ctx + kPageSize - 1) / kPageSize);
+    if (split_positions > 0) {
+        p->split_pages = split_positions / kPageSize;
+    } else {
+        int sms = 0;
+        int e = device_sm_count(&sms);
+        if (e != Q3KV_OK) return e;
+        const int64_t units = std::max<int64_t>(1, (int64_t)num_slots * d->num_kv_heads * p->row_chunks);
+        const int64_t target_splits = std::max<int64_t>(1, (2 * (int64_t)sms + units - 1) / units);
+        p->split_pages = (int)std::max<int64_t>(1, (pages + target_splits - 1) / target_splits);
+    }
+    p->num_splits = (int)((pages + p->split_pages - 1) / p->split_pages);
+    const int64_t units = (int64_t)std::max(num_slots, 1) * d->num_kv_heads * p->row_chunks;
+    p->part_o_bytes = (size_t)(units * p->num_splits * p->rows_per_chunk * kHeadDim) * sizeof(float);
+    p->part_ml_bytes = (size_t)(units * p->num_splits * p->rows_per_chunk * 2) * sizeof(float);
+    p->ticket_bytes = (size_t)((units * sizeof(int32_t) + 255) / 256 * 256);
+    if (p->num_splits == 1) p->part_o_bytes = p->part_ml_bytes = 0;
+    return Q3KV_OK;
+}
+
+}  // namespace
+
+struct q3kv_allocator {
+    int32_t num_pages;
+    int32_t num_slots;
+    int32_t max_pages_per_slot;
+    std::vector<int32_t> free_list;              // stack; back() is handed out next
+    std::vector<std::vector<int32_t>> owned;     // per-slot page ids in position order
+};
+
+extern "C" {
+
+int q3kv_version(void) { return kVersion; }
+int q3kv_format_version(void) { return Q3KV_FORMAT_VERSION; }
+
+const char* q3kv_strerror(int err) {
+    switch (err) {
+        case Q3KV_OK: return "ok";
+        case Q3KV_ERR_INVALID_ARG: return "invalid argument";
+        case Q3KV_ERR_UNSUPPORTED: return "unsupported shape or option";
+        case Q3KV_ERR_OUT_OF_PAGES: return "out of cache pages";
+        case Q3KV_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case Q3KV_ERR_CUDA: return "CUDA error";
+        case Q3KV_ERR_SLOT_RANGE: return "slot index out of range";
+        default: return "unknown error";
+    }
+}
+
+int q3kv_pool_bytes(const q3kv_cache_desc* desc, size_t* bytes) {
+    int e = check_desc(desc);
+    if (e != Q3KV_OK) return e;
+    if (!bytes) return Q3KV_ERR_INVALID_ARG;
+    *bytes = (size_t)desc->num_pages * desc->num_layers * desc->num_kv_heads * 2 * kPageSize * kRecordBytes;
+    return Q3KV_OK;
+}
+
+int q3kv_allocator_create(int32_t num_pages, int32_t num_slots, int32_t max_pages_per_slot, q3kv_allocator** out) {
+    if (!out || num_pages <= 0 || num_slots <= 0 || max_pages_per_slot <= 0) return Q3KV_ERR_INVALID_ARG;
+    q3kv_allocator* a = new (std::nothrow) q3kv_allocator();
+    if (!a) return Q3KV_ERR_INVALID_ARG;
+    a->num_pages = num_pages;
+    a->num_slots = num_slots;
+    a->max_pages_per_slot = max_pages_per_slot;
+    a->free_list.resize(num_pages);
+    for (int32_t i = 0; i < num_pages; ++i) a->free_list[i] = num_pages - 1 - i;   // page 0 first
+    a->owned.resize(num_slots);
+    *out = a;
+    return Q3KV_OK;
+}
+
+void q3kv_allocator_destroy(q3kv_allocator* a) { delete a; }
+
+int q3kv_alloc_pages(q3kv_allocator* a, int32_t slot, int64_t n_positions, int32_t* h_page_table_row,
+                     int32_t* n_pages_out) {
+    if (!a || !h_page_table_row || n_positions < 0) return Q3KV_ERR_INVALID_ARG;
+    if (slot < 0 || slot >= a->num_slots) return Q3KV_ERR_SLOT_RANGE;
+    const int64_t need = (n_positions + kPageSize - 1) / kPageSize;
+    if (need > a->max_pages_per_slot) return Q3KV_ERR_OUT_OF_PAGES;
+    std::vector<int32_t>& mine = a->owned[slot];
+    const int64_t extra = need - (int64_t)mine.size();
+    if (extra > (int64_t)a->free_list.size()) return Q3KV_ERR_OUT_OF_PAGES;
+    for (int64_t i = 0; i < extra; ++i) {
+        mine.push_back(a->free_list.back());
+        a->free_list.pop_back();
+    }
+    for (int32_t i = 0; i < a->max_pages_per_slot; ++i)
+        h_page_table_row[i] = (i < (int32_t)mine.size()) ? mine[i] : -1;
+    if (n_pages_out) *n_pages_out = (int32_t)mine.size();
+    return Q3KV_OK;
+}
+
+int q3kv_free_slot(q3kv_allocator* a, int32_t slot) {
+    if (!a) return Q3KV_ERR_INVALID_ARG;
+    if (slot < 0 || slot >= a->num_slots) return Q3KV_ERR_SLOT_RANGE;
+    std::vector<int32_t>& mine = a->owned[slot];
+    for (auto it = mine.rbegin(); it != mine.rend(); ++it) a->free_list.push_back(*it);
+    mine.clear();
+    return Q3KV_OK;
+}
+
+int q3kv_free_pages(const q3kv_allocator* a, int32_t* n_free) {
+    if (!a || !n_free) return Q3KV_ERR_INVALID_ARG;
+    *n_free = (int32_t)a->free_list.size();
+    return Q3KV_OK;
+}
+
+int q3kv_append(void* stream, const q3kv_cache_desc* desc, void* d_pool, const int32_t* d_page_table,
+                int32_t max_pages_per_slot, const int32_t* d_slot_len, const int32_t* d_n_new,
+                const int32_t* d_row_offsets, int32_t num_slots, int32_t max_n_new, int32_t layer, const void* k,
+                const void* v, int32_t dtype, int32_t* d_status) {
+    int e = check_desc(desc);
+    if (e != Q3KV_OK) return e;
+    if (num_slots < 0 || max_n_new < 0 || max_pages_per_slot <= 0) return Q3KV_ERR_INVALID_ARG;
+    if (num_slots > 65535) return Q3KV_ERR_UNSUPPORTED;
+    if (layer < 0 || layer >= desc->num_layers) return Q3KV_ERR_INVALID_ARG;
+    if (dtype != Q3KV_F32 && dtype != Q3KV_BF16) return Q3KV_ERR_INVALID_ARG;
+    if (num_slots == 0 || max_n_new == 0) return Q3KV_OK;
+    if (!d_pool || !d_page_table || !d_slot_len || !d_n_new || !d_row_offsets || !k || !v) return Q3KV_ERR_INVALID_ARG;
+    if (!aligned16(d_pool) || !aligned16(k) || !aligned16(v)) return Q3KV_ERR_INVALID_ARG;
+    AppendArgs a{};
+    a.pool = static_cast<uint8_t*>(d_pool);
+    a.page_table = d_page_table;
+    a.max_pages_per_slot = max_pages_per_slot;
+    a.slot_len = d_slot_len;
+    a.n_new = d_n_new;
+    a.row_offsets = d_row_offsets;
+    a.num_slots = num_slots;
+    a.max_n_new = max_n_new;
+    a.num_layers = desc->num_layers;
+    a.num_kv_heads = desc->num_kv_heads;
+    a.num_pages = desc->num_pages;
+    a.layer = layer;
+    a.k = k;
+    a.v = v;
+    a.dtype = dtype;
+    a.status = d_status;
+    return launch_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? Q3KV_OK : Q3KV_ERR_CUDA;
+}
+
+int q3kv_workspace_bytes(const q3kv_cache_desc* desc, int32_t num_slots, int64_t max_ctx_len, int32_t max_n_q,
+                         int32_t impl, int32_t split_positions, size_t* bytes) {
+    int e = check_desc(desc);
+    if (e != Q3KV_OK) return e;
+    if (!bytes) return Q3KV_ERR_INVALID_ARG;
+    Plan p;
+    e = make_plan(desc, num_slots, max_ctx_len, max_n_q, impl, split_positions, &p);
+    if (e != Q3KV_OK) return e;
+    *bytes = p.total();
+    return Q3KV_OK;
+}
+
+int q3kv_verify_attn(void* stream, const q3kv_cache_desc* desc, const void* d_pool, const int32_t* d_page_table,
+                     int32_t max_pages_per_slot, const int32_t* d_ctx_len, const int32_t* d_n_q,
+                     const int32_t* d_q_offsets, int32_t num_slots, int64_t max_ctx_len, int32_t max_n_q,
+                     int32_t layer, const void* q, int32_t dtype, float* out, int32_t impl,
+                     int32_t split_positions, void* d_workspace, size_t workspace_bytes, int32_t* d_status) {
+    int e = check_desc(desc);
+    if (e != Q3KV_OK) return e;
+    if (num_slots < 0 || max_pages_per_slot <= 0 || layer < 0 || layer >= desc->num_layers)
+        return Q3KV_ERR_INVALID_ARG;
+    if (num_slots > 65535) return Q3KV_ERR_UNSUPPORTED;
+    if (dtype != Q3KV_F32 && dtype != Q3KV_BF16) return Q3KV_ERR_INVALID_ARG;
+    if (max_n_q > kMaxNq) return Q3KV_ERR_UNSUPPORTED;
+    if (impl < Q3KV_IMPL_AUTO || impl > Q3KV_IMPL_MMA) return Q3KV_ERR_INVALID_ARG;
+    Plan p;
+    e = make_plan(desc, num_slots, max_ctx_len, max_n_q, impl, split_positions, &p);
+    if (e != Q3KV_OK) return e;
+    if (num_slots == 0 || max_n_q == 0 || max_ctx_len == 0) return Q3KV_OK;
+    if (!d_pool || !d_page_table || !d_ctx_len || !d_n_q || !d_q_offsets || !q || !out) return Q3KV_ERR_INVALID_ARG;
+    if (!aligned16(d_pool) || !aligned16(q) || !aligned16(out)) return Q3KV_ERR_INVALID_ARG;
+    if (workspace_bytes < p.total() || (p.total() > 0 && !d_workspace)) return Q3KV_ERR_WORKSPACE_TOO_SMALL;
+    if (d_workspace && !aligned16(d_workspace)) return Q3KV_ERR_INVALID_ARG;
+    if ((int64_t)p.num_splits > 65535) return Q3KV_ERR_UNSUPPORTED;
+
+    VerifyArgs a{};
+    a.pool = static_cast<const uint8_t*>(d_pool);
+    a.page_table = d_page_table;
+    a.max_pages_per_slot = max_pages_per_slot;
+    a.ctx_len = d_ctx_len;
+    a.n_q = d_n_q;
+    a.q_offsets = d_q_offsets;
+    a.num_slots = num_slots;
+    a.num_layers = desc->num_layers;
+    a.num_kv_heads = desc->num_kv_heads;
+    a.num_pages = desc->num_pages;
+    a.layer = layer;
+    a.q = q;
+    a.dtype = dtype;
+    a.out = out;
+    a.max_n_q = max_n_q;
+    a.split_pages = p.split_pages;
+    a.num_splits = p.num_splits;
+    a.row_chunks = p.row_chunks;
+    uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+    a.part_o = p.part_o_bytes ? reinterpret_cast<float*>(ws) : nullptr;
+    a.part_ml = p.part_ml_bytes ? reinterpret_cast<float*>(ws + p.part_o_bytes) : nullptr;
+    a.tickets = reinterpret_cast<int32_t*>(ws + p.part_o_bytes + p.part_ml_bytes);
+    a.status = d_status;
+    cudaError_t ce = launch_verify_fma(a, static_cast<cudaStream_t>(stream));
+    return ce == cudaSuccess ? Q3KV_OK : Q3KV_ERR_CUDA;
+}
+
+}  // extern "C"

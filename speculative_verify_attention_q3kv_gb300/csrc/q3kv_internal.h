@@ -1,0 +1,77 @@
+// Internal declarations shared by the host entry points and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/q3kv.h"
+
+namespace q3kv {
+
+constexpr int kHeadDim = 256;
+constexpr int kPageSize = 256;
+constexpr int kGroup = 8;            // q heads per kv head
+constexpr int kRecordBytes = 112;    // one coded vector
+constexpr int kCodeWords = 24;       // 96 bytes of codes
+constexpr int kMaxNq = 16;           // query tokens per slot and step
+constexpr int kMaxRows = kGroup * kMaxNq;
+
+// Byte offset of a record inside the pool (see q3kv_pool_bytes).
+__host__ __device__ inline size_t record_offset(int num_layers, int num_kv_heads, int64_t page,
+                                                int layer, int kv_head, int kv, int row) {
+    return (size_t)((((page * num_layers + layer) * num_kv_heads + kv_head) * 2 + kv) * kPageSize + row) *
+           kRecordBytes;
+}
+
+// Everything a verify launch needs, resolved on the host.
+struct VerifyArgs {
+    const uint8_t* pool;
+    const int32_t* page_table;
+    int32_t max_pages_per_slot;
+    const int32_t* ctx_len;
+    const int32_t* n_q;
+    const int32_t* q_offsets;
+    int32_t num_slots;
+    int32_t num_layers;
+    int32_t num_kv_heads;
+    int32_t num_pages;
+    int32_t layer;
+    const void* q;
+    int32_t dtype;
+    float* out;
+    int32_t max_n_q;
+    int32_t split_pages;       // pages per split-K unit
+    int32_t num_splits;        // splits of the longest slot
+    int32_t row_chunks;        // CTAs along the query rows of one kv head
+    float* part_o;             // [slots, kv_heads, row_chunks, splits, rows_per_chunk, 256]
+    float* part_ml;            // [slots, kv_heads, row_chunks, splits, rows_per_chunk, 2]
+    int32_t* tickets;          // [slots, kv_heads, row_chunks]
+    int32_t* status;
+};
+
+struct AppendArgs {
+    uint8_t* pool;
+    const int32_t* page_table;
+    int32_t max_pages_per_slot;
+    const int32_t* slot_len;
+    const int32_t* n_new;
+    const int32_t* row_offsets;
+    int32_t num_slots;
+    int32_t max_n_new;
+    int32_t num_layers;
+    int32_t num_kv_heads;
+    int32_t num_pages;
+    int32_t layer;
+    const void* k;
+    const void* v;
+    int32_t dtype;
+    int32_t* status;
+};
+
+// FMA (CUDA-core) leg: rows per CTA, and its workspace/launch.
+constexpr int kFmaRows = 64;
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
+cudaError_t launch_verify_fma(const VerifyArgs& a, cudaStream_t stream);
+
+}  // namespace q3kv

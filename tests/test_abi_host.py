@@ -1,0 +1,133 @@
+"""CPU tests of the C ABI: the library loads, exports every symbol the header
+declares, and its host logic (argument checks, pool sizing, workspace sizing,
+page allocator) behaves as documented.  No device work is launched."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from speculative_verify_attention_q3kv_gb300 import _lib, api
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q3kv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(q3kv_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert "q3kv_verify_attn" in names and "q3kv_append" in names and "q3kv_alloc_pages" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(_lib.PROTOTYPES)
+
+
+def test_header_constants_match_binding():
+    text = open(HEADER).read()
+    consts = dict((k, int(v)) for k, v in re.findall(r"#define\s+(Q3KV_[A-Z0-9_]+)\s+(-?\d+)", text))
+    for k, v in consts.items():
+        if hasattr(_lib, k):
+            assert getattr(_lib, k) == v, k
+
+
+def test_versions_and_strerror(lib):
+    assert lib.q3kv_version() >= 1
+    assert lib.q3kv_format_version() == 1
+    assert _lib.strerror(0) == "ok"
+    assert "page" in _lib.strerror(_lib.Q3KV_ERR_OUT_OF_PAGES)
+    assert _lib.strerror(12345) == "unknown error"
+
+
+def test_pool_bytes():
+    d = api.make_desc(16, 2, 2561)
+    assert api.pool_bytes(d) == 2561 * 16 * 2 * 2 * 256 * 112
+    bad = api.make_desc(16, 2, 10)
+    bad.head_dim = 128
+    with pytest.raises(_lib.Q3KVError) as e:
+        api.pool_bytes(bad)
+    assert e.value.code == _lib.Q3KV_ERR_UNSUPPORTED
+    bad = api.make_desc(16, 2, 10)
+    bad.num_q_heads = 12
+    with pytest.raises(_lib.Q3KVError):
+        api.pool_bytes(bad)
+    bad = api.make_desc(0, 2, 10)
+    with pytest.raises(_lib.Q3KVError) as e:
+        api.pool_bytes(bad)
+    assert e.value.code == _lib.Q3KV_ERR_INVALID_ARG
+
+
+def test_workspace_bytes_explicit_split():
+    d = api.make_desc(16, 2, 200)
+    # FMA leg, 1 slot, 32774 positions in 512-position splits, 6 tokens -> 48 rows in one 64-row chunk
+    n = api.workspace_bytes(d, 1, 32774, 6, _lib.Q3KV_IMPL_FMA, 512)
+    splits = -(-32774 // 512)
+    assert n >= 1 * 2 * splits * 64 * (256 + 2) * 4
+    with pytest.raises(_lib.Q3KVError):
+        api.workspace_bytes(d, 1, 1000, 6, _lib.Q3KV_IMPL_FMA, 300)     # not a page multiple
+    with pytest.raises(_lib.Q3KVError) as e:
+        api.workspace_bytes(d, 1, 1000, 17, _lib.Q3KV_IMPL_FMA, 256)    # more than 16 tokens
+    assert e.value.code == _lib.Q3KV_ERR_INVALID_ARG
+
+
+def test_allocator_lifecycle():
+    a = api.Allocator(num_pages=10, num_slots=3, max_pages_per_slot=6)
+    r0 = a.alloc_pages(0, 600)                     # 3 pages
+    assert list(r0[:3]) == [0, 1, 2] and np.all(r0[3:] == -1)
+    r1 = a.alloc_pages(1, 256)
+    assert list(r1[:1]) == [3]
+    r0b = a.alloc_pages(0, 700)                    # grows by 0 pages (still 3)
+    assert np.array_equal(r0, r0b)
+    r0c = a.alloc_pages(0, 769)                    # 4 pages
+    assert list(r0c[:4]) == [0, 1, 2, 4]
+    assert a.free_pages() == 5
+    with pytest.raises(_lib.Q3KVError) as e:
+        a.alloc_pages(2, 6 * 256 + 1)              # more than a row holds
+    assert e.value.code == _lib.Q3KV_ERR_OUT_OF_PAGES
+    a.alloc_pages(2, 5 * 256)                      # exactly the 5 left
+    assert a.free_pages() == 0
+    with pytest.raises(_lib.Q3KVError):
+        a.alloc_pages(1, 2 * 256)                  # all or nothing
+    assert a.free_pages() == 0
+    a.free_slot(0)
+    assert a.free_pages() == 4
+    r1b = a.alloc_pages(1, 3 * 256)
+    assert len(set(r1b[:3].tolist())) == 3 and r1b[0] == 3
+    with pytest.raises(_lib.Q3KVError) as e:
+        a.alloc_pages(3, 1)
+    assert e.value.code == _lib.Q3KV_ERR_SLOT_RANGE
+    a.close()
+
+
+def test_argument_checks_launch_nothing(lib):
+    d = api.make_desc(2, 2, 4)
+    # zero slots / zero tokens: OK and nothing launched (null pointers accepted)
+    assert lib.q3kv_append(None, ctypes.byref(d), None, None, 4, None, None, None, 0, 0, 0, None, None, 0, None) == 0
+    # a layer outside the pool
+    assert lib.q3kv_append(None, ctypes.byref(d), None, None, 4, None, None, None, 1, 1, 2, None, None, 0, None) == -1
+    # an unknown dtype
+    assert lib.q3kv_append(None, ctypes.byref(d), None, None, 4, None, None, None, 1, 1, 0, None, None, 7, None) == -1
+    # missing pointers with real work requested
+    assert lib.q3kv_append(None, ctypes.byref(d), None, None, 4, None, None, None, 1, 1, 0, None, None, 0, None) == -1
+    # verify: too many query tokens, an unknown impl, a too-small workspace
+    args = [None, ctypes.byref(d), None, None, 4, None, None, None, 1, 1000, 17, 0, None, 0, None, 1, 256, None, 0, None]
+    assert lib.q3kv_verify_attn(*args) == _lib.Q3KV_ERR_UNSUPPORTED
+    args[10] = 4
+    args[15] = 9
+    assert lib.q3kv_verify_attn(*args) == _lib.Q3KV_ERR_INVALID_ARG
+    buf = (ctypes.c_uint8 * 64)()
+    addr = ctypes.addressof(buf)
+    fake = (addr + 15) // 16 * 16
+    args[15] = 1
+    args[2] = args[3] = args[5] = args[6] = args[7] = args[12] = args[14] = fake
+    assert lib.q3kv_verify_attn(*args) == _lib.Q3KV_ERR_WORKSPACE_TOO_SMALL
