@@ -28,6 +28,8 @@ Q3KV_STATUS_NONFINITE_INPUT = 1
 Q3KV_STATUS_SCALE_OVERFLOW = 2
 Q3KV_STATUS_BAD_PAGE = 4
 Q3KV_STATUS_BAD_LENGTH = 8
+Q3KV_STATUS_TIMEOUT = 16
+Q3KV_STATUS_RANGE = 32
 
 Q3KV_F32 = 0
 Q3KV_BF16 = 1

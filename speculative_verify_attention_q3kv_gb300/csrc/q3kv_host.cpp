@@ -55,10 +55,10 @@ int make_plan(const q3kv_cache_desc* d, int32_t num_slots, int64_t max_ctx, int3
     if (num_slots < 0 || max_ctx < 0 || max_n_q < 0 || max_n_q > kMaxNq) return Q3KV_ERR_INVALID_ARG;
     if (split_positions < 0 || split_positions % kPageSize != 0) return Q3KV_ERR_INVALID_ARG;
     if (max_ctx > (int64_t)INT32_MAX - kPageSize) return Q3KV_ERR_INVALID_ARG;
-    if (impl == Q3KV_IMPL_AUTO) impl = Q3KV_IMPL_FMA;
-    if (impl != Q3KV_IMPL_FMA) return Q3KV_ERR_UNSUPPORTED;
+    if (impl == Q3KV_IMPL_AUTO) impl = Q3KV_IMPL_MMA;
+    if (impl != Q3KV_IMPL_FMA && impl != Q3KV_IMPL_MMA) return Q3KV_ERR_INVALID_ARG;
     p->impl = impl;
-    p->rows_per_chunk = kFmaRows;
+    p->rows_per_chunk = (impl == Q3KV_IMPL_MMA) ? kMmaRows : kFmaRows;
     const int rows = kGroup * std::max<int32_t>(max_n_q, 1);
     p->row_chunks = (rows + p->rows_per_chunk - 1) / p->rows_per_chunk;
     const int64_t pages = std::max<int64_t>(1, (max_ctx + kPageSize - 1) / kPageSize);
@@ -69,7 +69,10 @@ int make_plan(const q3kv_cache_desc* d, int32_t num_slots, int64_t max_ctx, int3
         int e = device_sm_count(&sms);
         if (e != Q3KV_OK) return e;
         const int64_t units = std::max<int64_t>(1, (int64_t)num_slots * d->num_kv_heads * p->row_chunks);
-        const int64_t target_splits = std::max<int64_t>(1, (2 * (int64_t)sms + units - 1) / units);
+        // FMA leg: about two CTAs per SM.  MMA leg (one CTA per SM): about two
+        // waves, so ragged slots still leave the SMs busy.
+        const int64_t target_ctas = 2 * (int64_t)sms;
+        const int64_t target_splits = std::max<int64_t>(1, (target_ctas + units - 1) / units);
         p->split_pages = (int)std::max<int64_t>(1, (pages + target_splits - 1) / target_splits);
     }
     p->num_splits = (int)((pages + p->split_pages - 1) / p->split_pages);
@@ -259,7 +262,8 @@ int q3kv_verify_attn(void* stream, const q3kv_cache_desc* desc, const void* d_po
     a.part_ml = p.part_ml_bytes ? reinterpret_cast<float*>(ws + p.part_o_bytes) : nullptr;
     a.tickets = reinterpret_cast<int32_t*>(ws + p.part_o_bytes + p.part_ml_bytes);
     a.status = d_status;
-    cudaError_t ce = launch_verify_fma(a, static_cast<cudaStream_t>(stream));
+    cudaError_t ce = (p.impl == Q3KV_IMPL_MMA) ? launch_verify_mma(a, static_cast<cudaStream_t>(stream))
+                                               : launch_verify_fma(a, static_cast<cudaStream_t>(stream));
     return ce == cudaSuccess ? Q3KV_OK : Q3KV_ERR_CUDA;
 }
 

@@ -73,5 +73,8 @@ struct AppendArgs {
 constexpr int kFmaRows = 64;
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_verify_fma(const VerifyArgs& a, cudaStream_t stream);
+// tcgen05 leg: 64 rows per CTA, one CTA per SM (shared memory bound).
+constexpr int kMmaRows = 64;
+cudaError_t launch_verify_mma(const VerifyArgs& a, cudaStream_t stream);
 
 }  // namespace q3kv

@@ -17,6 +17,7 @@
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
+#include "q3kv_common.cuh"
 #include "q3kv_internal.h"
 
 namespace q3kv {
@@ -37,9 +38,6 @@ struct FmaSmem {
     int flag;
 };
 
-__device__ __forceinline__ float load_in(const float* p) { return *p; }
-__device__ __forceinline__ float load_in(const __nv_bfloat16* p) { return __bfloat162float(*p); }
-
 // Decode the 32 codes of block b from its three words into (c - 3.5) * s.
 __device__ __forceinline__ void decode_block(const uint8_t* rec, int b, float* dst) {
     const uint32_t* w = reinterpret_cast<const uint32_t*>(rec) + 3 * b;
@@ -56,21 +54,6 @@ __device__ __forceinline__ void decode_block(const uint8_t* rec, int b, float* d
     const uint32_t c31 = ((w0 >> 31) & 1u) | (((w1 >> 31) & 1u) << 1) | (((w2 >> 31) & 1u) << 2);
     dst[30] = ((float)c30 - 3.5f) * s;
     dst[31] = ((float)c31 - 3.5f) * s;
-}
-
-// In-place H (unnormalised) on rows [0, nrows) of a [64][256] shared array.
-__device__ void rotate_rows(float (*x)[kHeadDim], int nrows) {
-    for (int h = 1; h < kHeadDim; h <<= 1) {
-        for (int idx = threadIdx.x; idx < nrows * (kHeadDim / 2); idx += kThreads) {
-            const int r = idx / (kHeadDim / 2);
-            const int j = idx % (kHeadDim / 2);
-            const int i = (j / h) * 2 * h + (j % h);
-            const float a = x[r][i], b = x[r][i + h];
-            x[r][i] = a + b;
-            x[r][i + h] = a - b;
-        }
-        __syncthreads();
-    }
 }
 
 template <typename TIn>
@@ -123,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_fma_kernel(VerifyArgs a) {
         sm.l_run[tid] = 0.0f;
     }
     __syncthreads();
-    rotate_rows(sm.q, Rc);
+    rotate_rows(&sm.q[0][0], Rc);
     for (int idx = tid; idx < Rc * kHeadDim; idx += kThreads) sm.q[idx / kHeadDim][idx % kHeadDim] *= (1.0f / 256.0f);
 
     float acc_o[16][4];
@@ -277,25 +260,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_fma_kernel(VerifyArgs a) {
         __syncthreads();
         if (!sm.flag) return;
         __threadfence();
-        // merge: thread = one output dim, loop rows
-        const float* po0 = a.part_o + (int64_t)unit * a.num_splits * kFmaRows * kHeadDim;
-        const float* pml0 = a.part_ml + (int64_t)unit * a.num_splits * kFmaRows * 2;
-        for (int r = 0; r < Rc; ++r) {
-            float M = -CUDART_INF_F;
-            for (int i = 0; i < n_splits; ++i) M = fmaxf(M, __ldcg(pml0 + ((int64_t)i * kFmaRows + r) * 2));
-            float lsum = 0.0f, o = 0.0f;
-            for (int i = 0; i < n_splits; ++i) {
-                const float mi = __ldcg(pml0 + ((int64_t)i * kFmaRows + r) * 2);
-                const float w = (mi == -CUDART_INF_F) ? 0.0f : expf(mi - M);
-                lsum += w * __ldcg(pml0 + ((int64_t)i * kFmaRows + r) * 2 + 1);
-                o += w * __ldcg(po0 + ((int64_t)i * kFmaRows + r) * kHeadDim + tid);
-            }
-            sm.q[r][tid] = o / lsum;
-        }
+        merge_splits<false>(a.part_o + (int64_t)unit * a.num_splits * kFmaRows * kHeadDim,
+                            a.part_ml + (int64_t)unit * a.num_splits * kFmaRows * 2, n_splits, Rc, kFmaRows,
+                            &sm.k[0][0], sm.m_run, sm.l_run, &sm.q[0][0]);
         if (tid == 0) a.tickets[unit] = 0;
     }
     __syncthreads();
-    rotate_rows(sm.q, Rc);
+    rotate_rows(&sm.q[0][0], Rc);
     for (int idx = tid; idx < Rc * kHeadDim; idx += kThreads) {
         const int r = idx / kHeadDim, d = idx % kHeadDim;
         const int ra = row0 + r;
