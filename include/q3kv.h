@@ -96,6 +96,10 @@ Q3KV_API int q3kv_format_version(void);
 /* Text of an error code (static string, never NULL). */
 Q3KV_API const char* q3kv_strerror(int err);
 
+/* Text of the last CUDA failure behind a Q3KV_ERR_CUDA return on the calling
+ * host thread (static string, never NULL). */
+Q3KV_API const char* q3kv_last_cuda_error(void);
+
 /* Bytes of a pool for desc:
  *   num_pages * num_layers * num_kv_heads * 2 * page_size * 112.
  * Pool layout: the 112-byte record of (page, layer, kv_head, kv in {0:K, 1:V},
@@ -165,9 +169,8 @@ Q3KV_API int q3kv_append(void* stream, const q3kv_cache_desc* desc, void* d_pool
  *   impl   Q3KV_IMPL_*;  split_positions: positions per split-K unit
  *          (multiple of 256; 0 = chosen from the shape and the GPU)
  *   workspace, workspace_bytes: device scratch of at least
- *          q3kv_workspace_bytes(...) bytes for the same arguments; it must be
- *          zero-filled once before first use (the kernels leave their merge
- *          counters at zero again when they finish).  Calls that share one
+ *          q3kv_workspace_bytes(...) bytes for the same arguments (split
+ *          partials; no initial contents needed).  Calls that share one
  *          workspace must not overlap on the GPU.
  * Slots with T_b == 0 produce nothing.  T_b > L_b or L_b beyond the slot's
  * page table sets Q3KV_STATUS_BAD_LENGTH and the slot's rows are left as they

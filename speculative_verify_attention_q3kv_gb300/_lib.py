@@ -51,6 +51,7 @@ PROTOTYPES = {
     "q3kv_version": (c_int32, []),
     "q3kv_format_version": (c_int32, []),
     "q3kv_strerror": (ctypes.c_char_p, [c_int32]),
+    "q3kv_last_cuda_error": (ctypes.c_char_p, []),
     "q3kv_pool_bytes": (c_int32, [P_desc, ctypes.POINTER(c_size_t)]),
     "q3kv_allocator_create": (c_int32, [c_int32, c_int32, c_int32, ctypes.POINTER(c_void_p)]),
     "q3kv_allocator_destroy": (None, [c_void_p]),
@@ -71,7 +72,10 @@ _LIB = None
 
 class Q3KVError(RuntimeError):
     def __init__(self, code: int, where: str):
-        super().__init__(f"{where}: {strerror(code)} ({code})")
+        detail = ""
+        if code == Q3KV_ERR_CUDA:
+            detail = ": " + load().q3kv_last_cuda_error().decode()
+        super().__init__(f"{where}: {strerror(code)} ({code}){detail}")
         self.code = code
 
 

@@ -16,6 +16,13 @@ using namespace q3kv;
 namespace {
 
 constexpr int kVersion = 1;
+thread_local cudaError_t g_last_cuda = cudaSuccess;   // last CUDA failure seen by this host thread
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return Q3KV_OK;
+    g_last_cuda = e;
+    return Q3KV_ERR_CUDA;
+}
 
 int check_desc(const q3kv_cache_desc* d) {
     if (!d) return Q3KV_ERR_INVALID_ARG;
@@ -31,9 +38,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int device_sm_count(int* sms) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return Q3KV_ERR_CUDA;
-    if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return Q3KV_ERR_CUDA;
-    return Q3KV_OK;
+    int e = cuda_status(cudaGetDevice(&dev));
+    if (e != Q3KV_OK) return e;
+    return cuda_status(cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev));
 }
 
 struct Plan {
@@ -44,8 +51,7 @@ struct Plan {
     int num_splits;
     size_t part_o_bytes;
     size_t part_ml_bytes;
-    size_t ticket_bytes;
-    size_t total() const { return part_o_bytes + part_ml_bytes + ticket_bytes; }
+    size_t total() const { return part_o_bytes + part_ml_bytes; }
 };
 
 // Split-K policy: enough (slot, kv head, row chunk, split) CTAs to cover the
@@ -79,7 +85,6 @@ int make_plan(const q3kv_cache_desc* d, int32_t num_slots, int64_t max_ctx, int3
     const int64_t units = (int64_t)std::max(num_slots, 1) * d->num_kv_heads * p->row_chunks;
     p->part_o_bytes = (size_t)(units * p->num_splits * p->rows_per_chunk * kHeadDim) * sizeof(float);
     p->part_ml_bytes = (size_t)(units * p->num_splits * p->rows_per_chunk * 2) * sizeof(float);
-    p->ticket_bytes = (size_t)((units * sizeof(int32_t) + 255) / 256 * 256);
     if (p->num_splits == 1) p->part_o_bytes = p->part_ml_bytes = 0;
     return Q3KV_OK;
 }
@@ -97,6 +102,10 @@ struct q3kv_allocator {
 extern "C" {
 
 int q3kv_version(void) { return kVersion; }
+
+const char* q3kv_last_cuda_error(void) {
+    return g_last_cuda == cudaSuccess ? "no CUDA error" : cudaGetErrorString(g_last_cuda);
+}
 int q3kv_format_version(void) { return Q3KV_FORMAT_VERSION; }
 
 const char* q3kv_strerror(int err) {
@@ -200,7 +209,7 @@ int q3kv_append(void* stream, const q3kv_cache_desc* desc, void* d_pool, const i
     a.v = v;
     a.dtype = dtype;
     a.status = d_status;
-    return launch_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? Q3KV_OK : Q3KV_ERR_CUDA;
+    return cuda_status(launch_append(a, static_cast<cudaStream_t>(stream)));
 }
 
 int q3kv_workspace_bytes(const q3kv_cache_desc* desc, int32_t num_slots, int64_t max_ctx_len, int32_t max_n_q,
@@ -235,6 +244,9 @@ int q3kv_verify_attn(void* stream, const q3kv_cache_desc* desc, const void* d_po
     if (!d_pool || !d_page_table || !d_ctx_len || !d_n_q || !d_q_offsets || !q || !out) return Q3KV_ERR_INVALID_ARG;
     if (!aligned16(d_pool) || !aligned16(q) || !aligned16(out)) return Q3KV_ERR_INVALID_ARG;
     if (workspace_bytes < p.total() || (p.total() > 0 && !d_workspace)) return Q3KV_ERR_WORKSPACE_TOO_SMALL;
+    if (p.num_splits > 1 && p.rows_per_chunk * (size_t)num_slots * desc->num_kv_heads * p.row_chunks > 0 &&
+        (size_t)num_slots * desc->num_kv_heads * p.row_chunks > 65535)
+        return Q3KV_ERR_UNSUPPORTED;
     if (d_workspace && !aligned16(d_workspace)) return Q3KV_ERR_INVALID_ARG;
     if ((int64_t)p.num_splits > 65535) return Q3KV_ERR_UNSUPPORTED;
 
@@ -260,11 +272,12 @@ int q3kv_verify_attn(void* stream, const q3kv_cache_desc* desc, const void* d_po
     uint8_t* ws = static_cast<uint8_t*>(d_workspace);
     a.part_o = p.part_o_bytes ? reinterpret_cast<float*>(ws) : nullptr;
     a.part_ml = p.part_ml_bytes ? reinterpret_cast<float*>(ws + p.part_o_bytes) : nullptr;
-    a.tickets = reinterpret_cast<int32_t*>(ws + p.part_o_bytes + p.part_ml_bytes);
     a.status = d_status;
-    cudaError_t ce = (p.impl == Q3KV_IMPL_MMA) ? launch_verify_mma(a, static_cast<cudaStream_t>(stream))
-                                               : launch_verify_fma(a, static_cast<cudaStream_t>(stream));
-    return ce == cudaSuccess ? Q3KV_OK : Q3KV_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool mma = (p.impl == Q3KV_IMPL_MMA);
+    cudaError_t ce = mma ? launch_verify_mma(a, st) : launch_verify_fma(a, st);
+    if (ce == cudaSuccess) ce = launch_merge(a, p.rows_per_chunk, mma, st);
+    return cuda_status(ce);
 }
 
 }  // extern "C"

@@ -46,7 +46,6 @@ struct VerifyArgs {
     int32_t row_chunks;        // CTAs along the query rows of one kv head
     float* part_o;             // [slots, kv_heads, row_chunks, splits, rows_per_chunk, 256]
     float* part_ml;            // [slots, kv_heads, row_chunks, splits, rows_per_chunk, 2]
-    int32_t* tickets;          // [slots, kv_heads, row_chunks]
     int32_t* status;
 };
 
@@ -76,5 +75,7 @@ cudaError_t launch_verify_fma(const VerifyArgs& a, cudaStream_t stream);
 // tcgen05 leg: 64 rows per CTA, one CTA per SM (shared memory bound).
 constexpr int kMmaRows = 64;
 cudaError_t launch_verify_mma(const VerifyArgs& a, cudaStream_t stream);
+// Split-K combine + inverse rotation (after either leg when num_splits > 1).
+cudaError_t launch_merge(const VerifyArgs& a, int rows_per_chunk, bool log2_units, cudaStream_t stream);
 
 }  // namespace q3kv

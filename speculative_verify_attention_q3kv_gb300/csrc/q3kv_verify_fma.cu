@@ -9,10 +9,9 @@
 // Rows of a kv head are r = t*8 + hh (token t, q head g*8 + hh), so the GQA
 // group and all drafted tokens share every K/V byte the CTA reads.  The CTA
 // walks its positions in tiles of 32: dequantise K and V into shared memory
-// (float32, exact), S = Q K^T on CUDA cores, online softmax, O += P V.  The
-// last CTA of a (slot, kv head, chunk) to finish merges the split partials
-//   o = sum_i e^(m_i - M) o_i / sum_i e^(m_i - M) l_i
-// and rotates the result back by H.
+// (float32, exact), S = Q K^T on CUDA cores, online softmax, O += P V.  With
+// one split the CTA rotates its result back by H and stores it; otherwise it
+// stores its partial (m, l, o) for the merge kernel.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>
@@ -35,7 +34,6 @@ struct FmaSmem {
     float m_run[kFmaRows];
     float l_run[kFmaRows];
     float alpha[kFmaRows];
-    int flag;
 };
 
 // Decode the 32 codes of block b from its three words into (c - 3.5) * s.
@@ -251,19 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_fma_kernel(VerifyArgs a) {
             pml[2 * tid] = sm.m_run[tid];
             pml[2 * tid + 1] = sm.l_run[tid];
         }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) {
-            const int prev = atomicAdd(a.tickets + unit, 1);
-            sm.flag = (prev == n_splits - 1);
-        }
-        __syncthreads();
-        if (!sm.flag) return;
-        __threadfence();
-        merge_splits<false>(a.part_o + (int64_t)unit * a.num_splits * kFmaRows * kHeadDim,
-                            a.part_ml + (int64_t)unit * a.num_splits * kFmaRows * 2, n_splits, Rc, kFmaRows,
-                            &sm.k[0][0], sm.m_run, sm.l_run, &sm.q[0][0]);
-        if (tid == 0) a.tickets[unit] = 0;
+        return;   // the merge kernel combines the splits
     }
     __syncthreads();
     rotate_rows(&sm.q[0][0], Rc);

@@ -9,7 +9,7 @@
 // adds error on top of the codec's, and the output tolerance here is tight.
 //
 // Work unit: one CTA = (slot, kv head, chunk of <= 64 query rows, split of the
-// context), 256 threads, positions in tiles of 128.
+// context), positions in tiles of 128.
 //
 // Precision.  The output must stay within 2e-3 of an fp64 reference, which a
 // single fp16 operand per side misses by 10-20x on outlier-heavy caches.  So
@@ -17,34 +17,40 @@
 //   K_hat = (c - 3.5) s = (c - 3.5) s_hi + (c - 3.5) s_lo, with s_hi = s rounded
 //           down to 8 significant bits; both products are exact in fp16;
 //   V_hat likewise; Q = Q_hi + Q_lo and P = P_hi + P_lo (round-to-nearest
-//   splits); and each contraction sums the three leading products
-//   (hi.hi + hi.lo + lo.hi) in fp32 tensor-core accumulation.
+//   splits); each contraction sums the three leading products
+//   (hi.hi + hi.lo + lo.hi) with fp32 accumulation in TMEM.
 //
-// Data flow of one tile (128 positions):
-//   1. thread 0 streams the tile's packed K and V records (2 x 14,336 B, one
-//      contiguous run each inside a page) into a 2-stage shared-memory ring
-//      with cp.async.bulk + mbarrier, two tiles ahead;
-//   2. all warps dequantise K_hat (hi, lo) straight into TMEM (lane =
-//      position), the A operand of S^T = K_hat Q^T (M = 128 positions,
-//      N = rows padded to 16, K = 256), B = Q (hi, lo) resident in shared
-//      memory, K-major;
-//   3. while the MMAs run, the warps dequantise V_hat for positions 0..63 into
-//      shared memory (MN-major A operand of O^T = V_hat^T P^T);
-//   4. softmax on S^T (thread = position): scores are in log2 units; the
-//      running row maximum is only raised when a score exceeds it by more
-//      than 8 (then the O^T accumulator columns are rescaled in TMEM), so the
-//      common tile needs no cross-lane maximum; P = 2^(s - m) <= 256 is split
-//      into fp16 hi/lo and stored MN-major as the B operand; row sums use a
-//      transposing butterfly (lane j ends with row j);
-//   5. O^T (two 128-lane halves of the 256 dims, fp32 in TMEM) += V_hat^T P^T
-//      for positions 0..63, then 64..127 after their V_hat is in place.
-// After the last tile each thread reads one output dim of O^T from TMEM.  The
-// split partials (m, l, o) are merged by the last CTA of the unit to finish,
-// which also rotates the result back by H.
+// Contractions (M = 128 for both):
+//   S^T[p][r] = K_hat[p][:] . Q[r][:]    A = K_hat in TMEM (lane = position),
+//                                        B = Q in shared memory (K-major),
+//                                        N = query rows padded to 16, K = 256
+//   O^T[d][r] += V_hat[:][d] . P[:][r]   A = V_hat^T in shared memory (MN-major),
+//                                        B = P^T in shared memory (MN-major),
+//                                        two 128-dim halves, K = 32 positions
+//
+// Warp roles (13 warps), each tile handed on with mbarriers:
+//   A  warps 0-3   softmax: thread = position; reads S^T from TMEM; scores
+//                  are in log2 units and the running row maximum is only
+//                  raised when a score exceeds it by more than 8 (then l and
+//                  the O^T columns are rescaled), so most tiles need no
+//                  cross-lane maximum; P = 2^(s - m) <= 256 goes to shared
+//                  memory as fp16 hi/lo; row sums by a transposing butterfly.
+//   B1 warps 4-7   K_hat of tile i+1 into TMEM as soon as the QK of tile i has
+//                  read it; also streams the K records (cp.async.bulk, two
+//                  tiles ahead).
+//   B2 warps 8-11  V_hat 32-position sub-tiles into two shared-memory buffers;
+//                  also streams the V records.
+//   M  warp 12     one thread issues every tcgen05.mma (QK of tile i+1 before
+//                  PV of tile i) and commits them to mbarriers.
+// TMEM (512 columns): K_hat hi | K_hat lo | S^T x 2 buffers | O^T x 2 halves.
+//
+// After the last tile the A warps read O^T (thread = two output dims) and
+// either finish the rows (one split: divide by l, rotate back by H) or store
+// the split partial (m, l, o) for the merge kernel.
 //
 // Every mbarrier wait is bounded (about a second); on a timeout the CTA sets
-// Q3KV_STATUS_TIMEOUT, stops issuing work, waits (bounded) for what it has in
-// flight, frees its TMEM and returns.
+// Q3KV_STATUS_TIMEOUT, stops, waits (bounded) for the copies and MMAs it has
+// in flight, frees its TMEM and returns.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>
@@ -55,9 +61,10 @@
 namespace q3kv {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kWarps = 13;
+constexpr int kThreads = kWarps * 32;
 constexpr int kTileP = 128;                 // positions per tile (MMA M of S^T)
-constexpr int kSubP = 64;                   // positions per V sub-tile
+constexpr int kSubP = 32;                   // positions per V sub-tile
 constexpr int kRows = 64;                   // max query rows per CTA (MMA N <= 64)
 constexpr int kStageBytes = kTileP * kRecordBytes;   // 14,336 B of K (or V) records
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P <= 256
@@ -67,29 +74,42 @@ constexpr float kMaxScale = 18688.0f;       // 3.5 * s must stay below the fp16 
 // TMEM columns (allocation of 512)
 constexpr uint32_t kColKHi = 0;
 constexpr uint32_t kColKLo = 128;
-constexpr uint32_t kColS = 256;
-constexpr uint32_t kColO0 = 320;
-constexpr uint32_t kColO1 = 384;
+constexpr uint32_t kColS = 256;             // + 64 * buffer
+constexpr uint32_t kColO0 = 384;
+constexpr uint32_t kColO1 = 448;
 constexpr uint32_t kTmemCols = 512;
+
+// named barriers
+constexpr int kBarA = 1;                    // the 128 softmax threads
+
+struct Bars {
+    unsigned long long full_k[2], full_v[2];   // records landed (tx bytes)
+    unsigned long long free_k[2], free_v[2];   // records read (4 warps each)
+    unsigned long long kready;                 // K_hat in TMEM (4 warps)
+    unsigned long long qk_done[2];             // S^T buffer written, K_hat read (commit)
+    unsigned long long s_free[2];              // S^T buffer read (4 warps)
+    unsigned long long p_ready;                // P^T stored, O^T rescaled (4 warps)
+    unsigned long long v_ready[4];             // V_hat of sub-tile s filled (1 warp)
+    unsigned long long v_free[4];              // V_hat of sub-tile s read (commit)
+    unsigned long long pv_done;                // all PV of a tile done (commit)
+    unsigned long long drain;                  // everything issued so far done (commit)
+};
 
 struct __align__(1024) MmaSmem {
     __half qhi[kRows * kHeadDim];           // B of QK, K-major core layout
     __half qlo[kRows * kHeadDim];
-    __half vhi[kSubP * kHeadDim];           // A of PV, MN-major core layout
-    __half vlo[kSubP * kHeadDim];
-    __half phi[kTileP * kRows];             // B of PV, MN-major core layout
+    __half v[2][2][kSubP * kHeadDim];       // [buffer][hi|lo]: A of PV, MN-major
+    __half phi[kTileP * kRows];             // B of PV, MN-major
     __half plo[kTileP * kRows];
-    uint8_t stage[2][2][kStageBytes];       // [stage][K|V][records]
+    uint8_t stage_k[2][kStageBytes];
+    uint8_t stage_v[2][kStageBytes];
     float m_run[kRows];
     float l_run[kRows];
     float alpha[kRows];
-    float red[8][32];
-    unsigned long long full_bar[2];
-    unsigned long long mma_bar;
+    int lim[kRows];
+    float red[4][kRows];
+    Bars bar;
     uint32_t tmem_base;
-    int tile_ok[2];
-    int issued[2];                          // tiles streamed into each stage so far
-    int flag;
     int abort;
 };
 
@@ -217,6 +237,35 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Named barrier among `n` threads (id 1.. ; id 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// OR of `pred` over the `n` threads of named barrier `id` (also a barrier).
+__device__ __forceinline__ int named_or(int id, int n, int pred) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.s32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.s32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(pred), "r"(id), "r"(n)
+        : "memory");
+    return r;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -240,12 +289,12 @@ __host__ __device__ constexpr uint32_t make_idesc(int n, bool a_mn_major, bool b
 // ---------------------------------------------------------------- layouts (element offsets)
 // Q (B of QK; N = rows r, K = dims k), K-major: core (r/8, k/8) at ((r/8)*32 + k/8)*64 elements.
 __device__ __forceinline__ int q_off(int r, int k) { return (((r >> 3) * 32 + (k >> 3)) << 6) + ((r & 7) << 3) + (k & 7); }
-// V_hat sub-tile (A of PV; M = dims d, K = positions p < 64), MN-major: core (d/8, p/8).
-__device__ __forceinline__ int v_off(int d, int p) { return (((d >> 3) * 8 + (p >> 3)) << 6) + ((p & 7) << 3) + (d & 7); }
+// V_hat sub-tile (A of PV; M = dims d, K = positions p < 32), MN-major: core (d/8, p/8).
+__device__ __forceinline__ int v_off(int d, int p) { return (((d >> 3) * 4 + (p >> 3)) << 6) + ((p & 7) << 3) + (d & 7); }
 // P^T (B of PV; N = rows r, K = positions p < 128), MN-major: core (r/8, p/8).
 __device__ __forceinline__ int p_off(int r, int p) { return (((r >> 3) * 16 + (p >> 3)) << 6) + ((p & 7) << 3) + (r & 7); }
 constexpr uint32_t kQLbo = 128, kQSbo = 32 * 128;
-constexpr uint32_t kVLbo = 128, kVSbo = 8 * 128;
+constexpr uint32_t kVLbo = 128, kVSbo = 4 * 128;
 constexpr uint32_t kPLbo = 128, kPSbo = 16 * 128;
 
 // ---------------------------------------------------------------- dequantisation
@@ -307,8 +356,53 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[32]) {
     return v[0];
 }
 
+__device__ __forceinline__ void load8(const float* src, float (&x)[8]) {
+    const float4 u = reinterpret_cast<const float4*>(src)[0];
+    const float4 w = reinterpret_cast<const float4*>(src)[1];
+    x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+    x[4] = w.x; x[5] = w.y; x[6] = w.z; x[7] = w.w;
+}
+
+__device__ __forceinline__ void load8(const __nv_bfloat16* src, float (&x)[8]) {
+    const uint4 u = reinterpret_cast<const uint4*>(src)[0];
+    const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(ww[i] << 16);
+        x[2 * i + 1] = __uint_as_float(ww[i] & 0xFFFF0000u);
+    }
+}
+
+// All lanes wait; the warp agrees on the outcome (a timeout anywhere fails all).
+__device__ __forceinline__ bool warp_wait(unsigned long long* bar, uint32_t parity, volatile int* abort) {
+    const bool ok = mbar_wait(bar, parity, abort);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Page of tile `it` of this split, or -1 if the page table entry is out of range.
+__device__ __forceinline__ int32_t tile_page(const VerifyArgs& a, const int32_t* pt_row, int pos0) {
+    const int32_t page = pt_row[pos0 / kPageSize];
+    return (page >= 0 && page < a.num_pages) ? page : -1;
+}
+
+// Load one 112-byte record from shared memory (7 x 16 bytes).
+__device__ __forceinline__ void load_record(const uint8_t* rec, uint32_t (&w)[24], uint32_t (&sc)[4]) {
+#pragma unroll
+    for (int k = 0; k < 6; ++k) {
+        const uint4 u = reinterpret_cast<const uint4*>(rec)[k];
+        w[4 * k] = u.x; w[4 * k + 1] = u.y; w[4 * k + 2] = u.z; w[4 * k + 3] = u.w;
+    }
+    const uint4 s = reinterpret_cast<const uint4*>(rec)[6];
+    sc[0] = s.x; sc[1] = s.y; sc[2] = s.z; sc[3] = s.w;
+}
+
+__device__ __forceinline__ __half scale_of(const uint32_t (&sc)[4], int b) {
+    const uint32_t u = sc[b >> 1];
+    return __ushort_as_half((unsigned short)((b & 1) ? (u >> 16) : (u & 0xFFFFu)));
+}
+
 template <typename TIn>
-__global__ void __launch_bounds__(kThreads, 1) verify_mma_kernel(VerifyArgs a) {
+__global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     MmaSmem& sm = *reinterpret_cast<MmaSmem*>(smem_raw);
     const int tid = threadIdx.x;
@@ -345,105 +439,288 @@ __global__ void __launch_bounds__(kThreads, 1) verify_mma_kernel(VerifyArgs a) {
     const int Hq = a.num_kv_heads * kGroup;
     const int64_t q_base = a.q_offsets[slot];
     const int N = (Rc + 15) & ~15;      // MMA N: rows padded to 16
-    const int Nh = N >> 1;              // columns per softmax warp half
-    const uint32_t idesc_qk = make_idesc(N, false, false);
-    const uint32_t idesc_pv = make_idesc(N, true, true);
     const int32_t* pt_row = a.page_table + (int64_t)slot * a.max_pages_per_slot;
     volatile int* abort = &sm.abort;
+    Bars& bar = sm.bar;
 
-    // ---- set-up: barriers, TMEM, queries
+    // ---- set-up: barriers, TMEM, row state, queries
     if (tid == 0) {
-        mbar_init(&sm.full_bar[0], 1);
-        mbar_init(&sm.full_bar[1], 1);
-        mbar_init(&sm.mma_bar, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bar.full_k[s], 1);
+            mbar_init(&bar.full_v[s], 1);
+            mbar_init(&bar.free_k[s], 4);
+            mbar_init(&bar.free_v[s], 4);
+            mbar_init(&bar.qk_done[s], 1);
+            mbar_init(&bar.s_free[s], 4);
+        }
+        for (int s = 0; s < 4; ++s) {
+            mbar_init(&bar.v_ready[s], 1);
+            mbar_init(&bar.v_free[s], 1);
+        }
+        mbar_init(&bar.kready, 4);
+        mbar_init(&bar.p_ready, 4);
+        mbar_init(&bar.pv_done, 1);
+        mbar_init(&bar.drain, 1);
         sm.abort = 0;
-        sm.issued[0] = sm.issued[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 0) tmem_alloc(&sm.tmem_base, kTmemCols);
+    if (warp == 12) tmem_alloc(&sm.tmem_base, kTmemCols);
     if (tid < kRows) {
         sm.m_run[tid] = -CUDART_INF_F;
         sm.l_run[tid] = 0.0f;
+        sm.lim[tid] = (tid < Rc) ? min(Nctx + (row0 + tid) / kGroup, p_end - 1) : -1;
     }
-    // raw queries -> fp32 scratch (the V_hat area), rows r = t*8 + hh of this chunk
-    float* qf = reinterpret_cast<float*>(sm.vhi);
-    const TIn* qin = static_cast<const TIn*>(a.q);
-    for (int idx = tid; idx < kRows * kHeadDim; idx += kThreads) {
-        const int r = idx / kHeadDim, d = idx % kHeadDim;
-        float x = 0.0f;
-        if (r < Rc) {
-            const int ra = row0 + r;
-            x = load_in(qin + ((q_base + ra / kGroup) * Hq + g * kGroup + ra % kGroup) * kHeadDim + d);
+    {   // queries: one warp per row, register butterflies for H, then scale
+        // 1/16 (H) * 1/16 (softmax) * log2(e) and split into fp16 hi + lo
+        const TIn* qin = static_cast<const TIn*>(a.q);
+        for (int r = warp; r < kRows; r += kWarps) {
+            float x[8];
+            if (r < Rc) {
+                const int ra = row0 + r;
+                load8(qin + ((q_base + ra / kGroup) * Hq + g * kGroup + ra % kGroup) * kHeadDim + 8 * lane, x);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] = 0.0f;
+            }
+#pragma unroll
+            for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if ((i & h) == 0) {
+                        const float lo = x[i], hi = x[i + h];
+                        x[i] = lo + hi;
+                        x[i + h] = lo - hi;
+                    }
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) {
+                const bool upper = (lane & m) != 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
+                    x[i] = upper ? o - x[i] : x[i] + o;
+                }
+            }
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float x0 = x[2 * i] * (1.4426950408889634f / 256.0f);
+                const float x1 = x[2 * i + 1] * (1.4426950408889634f / 256.0f);
+                const __half2 h2 = __floats2half2_rn(x0, x1);
+                const float2 hf = __half22float2(h2);
+                hw[i] = as_u32(h2);
+                lw[i] = as_u32(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
+            }
+            *reinterpret_cast<uint4*>(&sm.qhi[q_off(r, 8 * lane)]) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(&sm.qlo[q_off(r, 8 * lane)]) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
-        qf[idx] = x;
-    }
-    __syncthreads();
-    rotate_rows(qf, Rc);
-    // scale: 1/16 (H normalisation) * 1/16 (softmax) * log2(e); split into fp16 hi + lo
-    for (int idx = tid; idx < kRows * kHeadDim; idx += kThreads) {
-        const int r = idx / kHeadDim, d = idx % kHeadDim;
-        const float x = qf[idx] * (1.4426950408889634f / 256.0f);
-        const __half h = __float2half_rn(x);
-        const __half l = __float2half_rn(x - __half2float(h));
-        sm.qhi[q_off(r, d)] = h;
-        sm.qlo[q_off(r, d)] = l;
     }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
-
-    // ---- prologue: stream the first two tiles
-    auto issue_tile = [&](int it, int stg) {
-        const int pos0 = p_begin + it * kTileP;
-        const int32_t page = pt_row[pos0 / kPageSize];
-        if (page < 0 || page >= a.num_pages) {
-            sm.tile_ok[stg] = 0;
-            mbar_arrive(&sm.full_bar[stg]);
-            if (a.status) atomicOr(a.status, Q3KV_STATUS_BAD_PAGE);
-            return;
-        }
-        sm.tile_ok[stg] = 1;
-        sm.issued[stg] += 1;
-        const uint8_t* src_k = a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, 0, pos0 % kPageSize);
-        const uint8_t* src_v = a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, 1, pos0 % kPageSize);
-        mbar_arrive_expect_tx(&sm.full_bar[stg], 2 * kStageBytes);
-        bulk_g2s(sm.stage[stg][0], src_k, kStageBytes, &sm.full_bar[stg]);
-        bulk_g2s(sm.stage[stg][1], src_v, kStageBytes, &sm.full_bar[stg]);
-    };
-    if (tid == 0) {
-        issue_tile(0, 0);
-        if (n_tiles > 1) issue_tile(1, 1);
-    }
-
-    uint32_t mma_phase = 0;
-    int waited[2] = {0, 0};                 // tiles of each stage consumed
-    bool have_o = false;
     bool range_bad = false;
-    const int quarter = warp & 3;     // TMEM lane quarter of this warp
-    const int whalf = warp >> 2;      // 0: K dims 0..127 / S columns [0,Nh) / O dims 0..127
-    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    float* outs = reinterpret_cast<float*>(sm.qhi);      // [64][256] floats once Q is no longer read
 
-    for (int it = 0; it < n_tiles; ++it) {
-        const int stg = it & 1;
-        const int pos0 = p_begin + it * kTileP;
-        mbar_wait(&sm.full_bar[stg], (uint32_t)((it >> 1) & 1), abort);
-        const bool tile_ok = sm.tile_ok[stg] != 0;
-
-        // (2) K_hat -> TMEM: position 32*quarter + lane, blocks 4*whalf .. 4*whalf+3
-        {
-            const int p = quarter * 32 + lane;
-            const bool valid = tile_ok && (pos0 + p) < p_end;
-            const uint8_t* rec = sm.stage[stg][0] + p * kRecordBytes;
-            const __half* sc = reinterpret_cast<const __half*>(rec + 96);
+    if (warp < 4) {
+        // ================================================================ A: softmax
+        const int q = warp;
+        const int p = 32 * q + lane;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        bool ok = true;
+        for (int i = 0; i < n_tiles; ++i) {
+            const int b = i & 1;
+            ok = ok && mbar_wait(&bar.qk_done[b], (uint32_t)((i >> 1) & 1), abort);
+            tc_fence_after();
+            float x[kRows];
 #pragma unroll
-            for (int bb = 0; bb < 4; ++bb) {
-                const int b = whalf * 4 + bb;
+            for (int c = 0; c < 4; ++c) {
+                if (16 * c < N) tmem_ld16(tmem + lane_base + kColS + 64 * b + 16 * c, &x[16 * c]);
+            }
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.s_free[b]);
+
+            const int pos0 = p_begin + i * kTileP;
+            const int pos = pos0 + p;
+            const bool tile_ok = tile_page(a, pt_row, pos0) >= 0;
+            const bool interior = tile_ok && pos0 + kTileP - 1 <= min(Nctx, p_end - 1);
+            int over = 0;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const float4 m4 = reinterpret_cast<const float4*>(sm.m_run)[c];
+                const int4 l4 = reinterpret_cast<const int4*>(sm.lim)[c];
+                const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+                const int ll[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int j = 4 * c + k;
+                    float v = x[j];
+                    if (j >= N) v = -CUDART_INF_F;
+                    else if (!interior && !(tile_ok && pos <= ll[k])) v = -CUDART_INF_F;
+                    x[j] = v;
+                    over |= (v > mm[k] + kRescaleThreshold) ? 1 : 0;
+                }
+            }
+            const int slow = named_or(kBarA, 128, over);
+            if (slow) {
+                // raise the running maxima to cover this tile; rescale l (O below)
+#pragma unroll
+                for (int j = 0; j < kRows; ++j) {
+                    if (j < N) {
+                        float mx = x[j];
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                        if (lane == 0) sm.red[q][j] = mx;
+                    }
+                }
+                named_sync(kBarA, 128);
+                if (tid < N) {
+                    const float mt = fmaxf(fmaxf(sm.red[0][tid], sm.red[1][tid]), fmaxf(sm.red[2][tid], sm.red[3][tid]));
+                    const float m_old = sm.m_run[tid];
+                    const float m_new = fmaxf(m_old, mt);
+                    const float al = (m_old == -CUDART_INF_F) ? 0.0f : exp2f(m_old - m_new);
+                    sm.m_run[tid] = m_new;
+                    sm.l_run[tid] *= al;
+                    sm.alpha[tid] = al;
+                }
+                named_sync(kBarA, 128);
+            }
+            // P = 2^(s - m) in place
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const float4 m4 = reinterpret_cast<const float4*>(sm.m_run)[c];
+                const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int j = 4 * c + k;
+                    x[j] = (x[j] == -CUDART_INF_F) ? 0.0f : fast_exp2(x[j] - mm[k]);
+                }
+            }
+            // the previous tile's PV must be finished before P^T and O^T change
+            if (i > 0) ok = ok && mbar_wait(&bar.pv_done, (uint32_t)((i - 1) & 1), abort);
+            if (slow && i > 0) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t col = h ? kColO1 : kColO0;
+#pragma unroll 1
+                    for (int c = 0; c < N; c += 8) {
+                        float v8[8];
+                        tmem_ld8(tmem + lane_base + col + c, v8);
+                        tmem_ld_wait();
+                        uint32_t u8[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) u8[k] = __float_as_uint(v8[k] * sm.alpha[c + k]);
+                        tmem_st8(tmem + lane_base + col + c, u8);
+                    }
+                }
+                tmem_st_wait();
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                if (8 * c < N) {
+                    uint32_t h4[4], l4[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float a0 = x[8 * c + 2 * k], a1 = x[8 * c + 2 * k + 1];
+                        const __half2 hh2 = __floats2half2_rn(a0, a1);
+                        const float2 hf = __half22float2(hh2);
+                        h4[k] = as_u32(hh2);
+                        l4[k] = as_u32(__floats2half2_rn(a0 - hf.x, a1 - hf.y));
+                    }
+                    *reinterpret_cast<uint4*>(&sm.phi[p_off(8 * c, p)]) = make_uint4(h4[0], h4[1], h4[2], h4[3]);
+                    *reinterpret_cast<uint4*>(&sm.plo[p_off(8 * c, p)]) = make_uint4(l4[0], l4[1], l4[2], l4[3]);
+                }
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.p_ready);
+            // row sums of this tile
+            sm.red[q][lane] = transpose_reduce<false>(*reinterpret_cast<float(*)[32]>(&x[0]));
+            if (N > 32) sm.red[q][32 + lane] = transpose_reduce<false>(*reinterpret_cast<float(*)[32]>(&x[32]));
+            named_sync(kBarA, 128);
+            if (tid < N) sm.l_run[tid] += (sm.red[0][tid] + sm.red[1][tid]) + (sm.red[2][tid] + sm.red[3][tid]);
+        }
+        named_sync(kBarA, 128);   // l_run complete
+        // ---- epilogue: O^T -> partial or finished rows
+        ok = ok && mbar_wait(&bar.pv_done, (uint32_t)((n_tiles - 1) & 1), abort);
+        tc_fence_after();
+        if (ok) {
+            const int unit = (slot * a.num_kv_heads + g) * a.row_chunks + chunk;
+            float* po = a.part_o + ((int64_t)unit * a.num_splits + split) * kRows * kHeadDim;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                const int d = 128 * h + 32 * q + lane;
+                const uint32_t col = h ? kColO1 : kColO0;
+#pragma unroll 1
+                for (int c = 0; c < N; c += 16) {
+                    float v16[16];
+                    tmem_ld16(tmem + lane_base + col + c, v16);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const int r = c + k;
+                        if (r < Rc) {
+                            if (n_splits == 1) outs[r * kHeadDim + d] = v16[k] / sm.l_run[r];
+                            else po[r * kHeadDim + d] = v16[k];
+                        }
+                    }
+                }
+            }
+            if (n_splits > 1 && tid < Rc) {
+                float* pml = a.part_ml + ((int64_t)unit * a.num_splits + split) * kRows * 2;
+                pml[2 * tid] = sm.m_run[tid];
+                pml[2 * tid + 1] = sm.l_run[tid];
+            }
+        }
+    } else if (warp < 8) {
+        // ================================================================ B1: K_hat -> TMEM
+        const int q = warp - 4;
+        const int p = 32 * q + lane;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const bool producer = (warp == 4 && lane == 0);
+        int issued = 0, consumed = 0;
+        auto issue = [&](int it) {
+            const int stg = it & 1;
+            const int pos0 = p_begin + it * kTileP;
+            const int32_t page = tile_page(a, pt_row, pos0);
+            if (page < 0) {
+                if (a.status) atomicOr(a.status, Q3KV_STATUS_BAD_PAGE);
+                mbar_arrive(&bar.full_k[stg]);
+            } else {
+                mbar_arrive_expect_tx(&bar.full_k[stg], kStageBytes);
+                bulk_g2s(sm.stage_k[stg], a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, 0,
+                                                                 pos0 % kPageSize),
+                         kStageBytes, &bar.full_k[stg]);
+            }
+        };
+        if (producer) {
+            issue(0);
+            if (n_tiles > 1) issue(1);
+        }
+        issued = min(n_tiles, 2);
+        for (int i = 0; i < n_tiles; ++i) {
+            const int stg = i & 1;
+            if (!warp_wait(&bar.full_k[stg], (uint32_t)((i >> 1) & 1), abort)) break;
+            consumed = i + 1;
+            if (i > 0 && !warp_wait(&bar.qk_done[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1), abort)) break;
+            tc_fence_after();
+            const int pos0 = p_begin + i * kTileP;
+            const bool valid = tile_page(a, pt_row, pos0) >= 0 && pos0 + p < p_end;
+            uint32_t w[24], sc[4];
+            load_record(sm.stage_k[stg] + p * kRecordBytes, w, sc);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.free_k[stg]);
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
                 uint32_t hi[16], lo[16];
+                const __half s = scale_of(sc, b);
                 if (valid) {
-                    dequant_block(reinterpret_cast<const uint32_t*>(rec) + 3 * b, sc[b], hi, lo);
-                    range_bad |= !(__half2float(sc[b]) <= kMaxScale);
+                    dequant_block(&w[3 * b], s, hi, lo);
+                    range_bad |= !(__half2float(s) <= kMaxScale);
                 } else {
 #pragma unroll
                     for (int m = 0; m < 16; ++m) hi[m] = lo[m] = 0u;
@@ -452,276 +729,183 @@ __global__ void __launch_bounds__(kThreads, 1) verify_mma_kernel(VerifyArgs a) {
                 tmem_st16(tmem + lane_base + kColKLo + 16 * b, lo);
             }
             tmem_st_wait();
-        }
-        tc_fence_before();
-        __syncthreads();
-
-        // (2b) QK MMAs: S^T[p][r] = sum_k K[p][k] Q[r][k]
-        if (tid == 0 && !*abort) {
-            tc_fence_after();
-            const uint32_t qh = smem_u32(sm.qhi), ql = smem_u32(sm.qlo);
-#pragma unroll 1
-            for (int j = 0; j < 16; ++j) {
-                const uint64_t bh = make_desc(qh + j * 256, kQLbo, kQSbo);
-                const uint64_t bl = make_desc(ql + j * 256, kQLbo, kQSbo);
-                mma_ts(tmem + kColS, tmem + kColKHi + 8 * j, bh, idesc_qk, j > 0 ? 1u : 0u);
-                mma_ts(tmem + kColS, tmem + kColKHi + 8 * j, bl, idesc_qk, 1u);
-                mma_ts(tmem + kColS, tmem + kColKLo + 8 * j, bh, idesc_qk, 1u);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.kready);
+            if (warp == 4 && i + 2 < n_tiles) {
+                if (!warp_wait(&bar.free_k[stg], (uint32_t)((i >> 1) & 1), abort)) break;
+                if (producer) issue(i + 2);
+                issued = i + 3;
+                __syncwarp();
             }
-            mma_commit(&sm.mma_bar);
         }
-
-        // (3) V_hat positions 0..63 -> shared memory while the MMAs run
-        auto dequant_v = [&](int sub) {
-            const int pl = tid & 63;                 // position within the sub-tile
-            const int p = sub * kSubP + pl;          // position within the tile
-            const bool valid = tile_ok && (pos0 + p) < p_end;
-            const uint8_t* rec = sm.stage[stg][1] + p * kRecordBytes;
-            const __half* sc = reinterpret_cast<const __half*>(rec + 96);
+        if (producer && *abort)
+            for (int t = consumed; t < issued; ++t) mbar_drain(&bar.full_k[t & 1], (uint32_t)((t >> 1) & 1));
+    } else if (warp < 12) {
+        // ================================================================ B2: V_hat sub-tiles -> shared memory
+        const int q = warp - 8;                      // sub-tile q of every tile
+        const int buf = q & 1;
+        const bool producer = (warp == 8 && lane == 0);
+        int issued = 0, consumed = 0;
+        auto issue = [&](int it) {
+            const int stg = it & 1;
+            const int pos0 = p_begin + it * kTileP;
+            const int32_t page = tile_page(a, pt_row, pos0);
+            if (page < 0) {
+                mbar_arrive(&bar.full_v[stg]);
+            } else {
+                mbar_arrive_expect_tx(&bar.full_v[stg], kStageBytes);
+                bulk_g2s(sm.stage_v[stg], a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, 1,
+                                                                 pos0 % kPageSize),
+                         kStageBytes, &bar.full_v[stg]);
+            }
+        };
+        if (producer) {
+            issue(0);
+            if (n_tiles > 1) issue(1);
+        }
+        issued = min(n_tiles, 2);
+        for (int i = 0; i < n_tiles; ++i) {
+            const int stg = i & 1;
+            if (!warp_wait(&bar.full_v[stg], (uint32_t)((i >> 1) & 1), abort)) break;
+            consumed = i + 1;
+            // buffer q & 1 was last read by PV(i, q - 2) or PV(i - 1, q + 2); each
+            // sub-tile has its own barrier pair, so every waiter sees every phase
+            if (q >= 2) {
+                if (!warp_wait(&bar.v_free[q - 2], (uint32_t)(i & 1), abort)) break;
+            } else if (i >= 1) {
+                if (!warp_wait(&bar.v_free[q + 2], (uint32_t)((i - 1) & 1), abort)) break;
+            }
+            const int pos0 = p_begin + i * kTileP;
+            const int pt = 32 * q + lane;
+            const bool valid = tile_page(a, pt_row, pos0) >= 0 && pos0 + pt < p_end;
+            uint32_t w[24], sc[4];
+            load_record(sm.stage_v[stg] + pt * kRecordBytes, w, sc);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.free_v[stg]);
+            __half* vh = sm.v[buf][0];
+            __half* vl = sm.v[buf][1];
 #pragma unroll
-            for (int bb = 0; bb < 2; ++bb) {
-                const int b = (tid >> 6) * 2 + bb;
+            for (int b = 0; b < 8; ++b) {
                 uint32_t hi[16], lo[16];
+                const __half s = scale_of(sc, b);
                 if (valid) {
-                    dequant_block(reinterpret_cast<const uint32_t*>(rec) + 3 * b, sc[b], hi, lo);
-                    range_bad |= !(__half2float(sc[b]) <= kMaxScale);
+                    dequant_block(&w[3 * b], s, hi, lo);
+                    range_bad |= !(__half2float(s) <= kMaxScale);
                 } else {
 #pragma unroll
                     for (int m = 0; m < 16; ++m) hi[m] = lo[m] = 0u;
                 }
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {          // 8 dims per 16-byte chunk
+                for (int c = 0; c < 4; ++c) {
                     const int d0 = 32 * b + 8 * c;
-                    *reinterpret_cast<uint4*>(&sm.vhi[v_off(d0, pl)]) =
+                    *reinterpret_cast<uint4*>(&vh[v_off(d0, lane)]) =
                         make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
-                    *reinterpret_cast<uint4*>(&sm.vlo[v_off(d0, pl)]) =
+                    *reinterpret_cast<uint4*>(&vl[v_off(d0, lane)]) =
                         make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
                 }
             }
             fence_proxy_async();
-        };
-        dequant_v(0);
-
-        if (mbar_wait(&sm.mma_bar, mma_phase, abort)) mma_phase ^= 1;
-        tc_fence_after();
-
-        // (4) softmax: thread = position 32*quarter + lane; rows [whalf*Nh, whalf*Nh + Nh)
-        {
-            const int p = quarter * 32 + lane;
-            const int pos = pos0 + p;
-            const bool valid = tile_ok && pos < p_end;
-            float x[32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (8 * c < Nh) {
-                    float v8[8];
-                    tmem_ld8(tmem + lane_base + kColS + whalf * Nh + 8 * c, v8);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) x[8 * c + i] = v8[i];
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) x[8 * c + i] = -CUDART_INF_F;
-                }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.v_ready[q]);
+            if (warp == 8 && i + 2 < n_tiles) {
+                if (!warp_wait(&bar.free_v[stg], (uint32_t)((i >> 1) & 1), abort)) break;
+                if (producer) issue(i + 2);
+                issued = i + 3;
+                __syncwarp();
             }
-            tmem_ld_wait();
-            int over = 0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int r = whalf * Nh + j;
-                const bool vis = valid && j < Nh && r < Rc && pos <= Nctx + (row0 + r) / kGroup;
-                x[j] = vis ? x[j] : -CUDART_INF_F;
-                if (vis && x[j] > sm.m_run[r] + kRescaleThreshold) over = 1;
-            }
-            if (__syncthreads_or(over)) {
-                // raise the running maxima to the tile maxima, rescale l and O
-                float t[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) t[j] = x[j];
-                const float mx = transpose_reduce<true>(t);
-                sm.red[warp][lane] = mx;
-                __syncthreads();
-                if (tid < N) {
-                    const int hh = tid / Nh, j = tid % Nh;
-                    float mt = -CUDART_INF_F;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) mt = fmaxf(mt, sm.red[hh * 4 + q][j]);
-                    const float m_old = sm.m_run[tid];
-                    const float m_new = fmaxf(m_old, mt);
-                    const float al = (m_old == -CUDART_INF_F) ? 0.0f : exp2f(m_old - m_new);
-                    sm.m_run[tid] = m_new;
-                    sm.l_run[tid] *= al;
-                    sm.alpha[tid] = al;
-                }
-                __syncthreads();
-                if (have_o) {
-                    const uint32_t col = whalf ? kColO1 : kColO0;
-                    for (int c = 0; c < N; c += 8) {
-                        float v8[8];
-                        tmem_ld8(tmem + lane_base + col + c, v8);
-                        tmem_ld_wait();
-                        uint32_t u8[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) u8[i] = __float_as_uint(v8[i] * sm.alpha[c + i]);
-                        tmem_st8(tmem + lane_base + col + c, u8);
-                    }
-                    tmem_st_wait();
-                }
-            }
-            // P = 2^(s - m), split hi/lo, store P^T; row sums
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int r = whalf * Nh + j;
-                const float m = (j < Nh) ? sm.m_run[min(r, kRows - 1)] : 0.0f;
-                x[j] = (x[j] == -CUDART_INF_F) ? 0.0f : fast_exp2(x[j] - m);
-            }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (8 * c < Nh) {
-                    uint32_t h4[4], l4[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float a0 = x[8 * c + 2 * i], a1 = x[8 * c + 2 * i + 1];
-                        const __half2 hh2 = __floats2half2_rn(a0, a1);
-                        const float2 hf = __half22float2(hh2);
-                        const __half2 ll2 = __floats2half2_rn(a0 - hf.x, a1 - hf.y);
-                        h4[i] = as_u32(hh2);
-                        l4[i] = as_u32(ll2);
-                    }
-                    const int r0 = whalf * Nh + 8 * c;
-                    *reinterpret_cast<uint4*>(&sm.phi[p_off(r0, p)]) = make_uint4(h4[0], h4[1], h4[2], h4[3]);
-                    *reinterpret_cast<uint4*>(&sm.plo[p_off(r0, p)]) = make_uint4(l4[0], l4[1], l4[2], l4[3]);
-                }
-            }
-            fence_proxy_async();
-            const float ls = transpose_reduce<false>(x);
-            sm.red[warp][lane] = ls;
         }
-        tc_fence_before();
-        __syncthreads();
-        if (tid < N) {
-            const int hh = tid / Nh, j = tid % Nh;
-            float s = 0.0f;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) s += sm.red[hh * 4 + q][j];
-            sm.l_run[tid] += s;
-        }
-
-        // (5) PV, positions 0..63
-        auto issue_pv = [&](int sub) {
-            tc_fence_after();
-            const uint32_t vh = smem_u32(sm.vhi), vl = smem_u32(sm.vlo);
-            const uint32_t ph = smem_u32(sm.phi), pl = smem_u32(sm.plo);
+        if (producer && *abort)
+            for (int t = consumed; t < issued; ++t) mbar_drain(&bar.full_v[t & 1], (uint32_t)((t >> 1) & 1));
+    } else {
+        // ================================================================ M: MMA issue
+        const uint32_t idesc_qk = make_idesc(N, false, false);
+        const uint32_t idesc_pv = make_idesc(N, true, true);
+        const uint32_t qh = smem_u32(sm.qhi), ql = smem_u32(sm.qlo);
+        const uint32_t ph = smem_u32(sm.phi), pl = smem_u32(sm.plo);
+        for (int i = 0; i <= n_tiles; ++i) {
+            if (i < n_tiles) {
+                const int b = i & 1;
+                if (!warp_wait(&bar.kready, (uint32_t)(i & 1), abort)) break;
+                if (i >= 2 && !warp_wait(&bar.s_free[b], (uint32_t)(((i >> 1) - 1) & 1), abort)) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t dS = tmem + kColS + 64 * b;
 #pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t dcol = tmem + (h ? kColO1 : kColO0);
-#pragma unroll 1
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t aoff = (uint32_t)(16 * h) * kVSbo + (uint32_t)(2 * j) * kVLbo;
-                    const uint32_t boff = (uint32_t)(8 * sub + 2 * j) * kPLbo;
-                    const uint64_t avh = make_desc(vh + aoff, kVLbo, kVSbo);
-                    const uint64_t avl = make_desc(vl + aoff, kVLbo, kVSbo);
-                    const uint64_t bph = make_desc(ph + boff, kPLbo, kPSbo);
-                    const uint64_t bpl = make_desc(pl + boff, kPLbo, kPSbo);
-                    const uint32_t acc0 = (have_o || sub > 0 || j > 0) ? 1u : 0u;
-                    mma_ss(dcol, avh, bph, idesc_pv, acc0);
-                    mma_ss(dcol, avl, bph, idesc_pv, 1u);
-                    mma_ss(dcol, avh, bpl, idesc_pv, 1u);
+                    for (int j = 0; j < 16; ++j) {
+                        const uint64_t bh = make_desc(qh + j * 256, kQLbo, kQSbo);
+                        const uint64_t bl = make_desc(ql + j * 256, kQLbo, kQSbo);
+                        mma_ts(dS, tmem + kColKHi + 8 * j, bh, idesc_qk, j > 0 ? 1u : 0u);
+                        mma_ts(dS, tmem + kColKHi + 8 * j, bl, idesc_qk, 1u);
+                        mma_ts(dS, tmem + kColKLo + 8 * j, bh, idesc_qk, 1u);
+                    }
+                    mma_commit(&bar.qk_done[b]);
                 }
+                __syncwarp();
             }
-            mma_commit(&sm.mma_bar);
-        };
-        if (tid == 0 && !*abort) issue_pv(0);
-        if (mbar_wait(&sm.mma_bar, mma_phase, abort)) mma_phase ^= 1;
-
-        // V_hat positions 64..127 (the V buffer is free again), then PV for them
-        dequant_v(1);
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0 && !*abort) {
-            issue_pv(1);
-            if (it + 2 < n_tiles) issue_tile(it + 2, stg);   // this stage is fully consumed
+            if (i >= 1) {
+                const int jt = i - 1;                  // PV of the previous tile
+                if (!warp_wait(&bar.p_ready, (uint32_t)(jt & 1), abort)) break;
+                bool ok = true;
+#pragma unroll 1
+                for (int s = 0; s < 4 && ok; ++s) {
+                    const int vb = s & 1;
+                    ok = warp_wait(&bar.v_ready[s], (uint32_t)(jt & 1), abort);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t vh = smem_u32(sm.v[vb][0]), vl = smem_u32(sm.v[vb][1]);
+#pragma unroll 1
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t dO = tmem + (h ? kColO1 : kColO0);
+#pragma unroll 1
+                            for (int j = 0; j < 2; ++j) {
+                                const uint32_t aoff = (uint32_t)(16 * h) * kVSbo + (uint32_t)(2 * j) * kVLbo;
+                                const uint32_t boff = (uint32_t)(4 * s + 2 * j) * kPLbo;
+                                const uint64_t avh = make_desc(vh + aoff, kVLbo, kVSbo);
+                                const uint64_t avl = make_desc(vl + aoff, kVLbo, kVSbo);
+                                const uint64_t bph = make_desc(ph + boff, kPLbo, kPSbo);
+                                const uint64_t bpl = make_desc(pl + boff, kPLbo, kPSbo);
+                                const uint32_t acc0 = (jt > 0 || s > 0 || j > 0) ? 1u : 0u;
+                                mma_ss(dO, avh, bph, idesc_pv, acc0);
+                                mma_ss(dO, avl, bph, idesc_pv, 1u);
+                                mma_ss(dO, avh, bpl, idesc_pv, 1u);
+                            }
+                        }
+                        mma_commit(&bar.v_free[s]);
+                    }
+                    __syncwarp();
+                }
+                if (!ok) break;
+                if (lane == 0) mma_commit(&bar.pv_done);
+                __syncwarp();
+            }
         }
-        have_o = true;
-        if (mbar_wait(&sm.mma_bar, mma_phase, abort)) mma_phase ^= 1;
-        tc_fence_after();
-        waited[stg] += 1;
+        // wait for every MMA this thread issued (bounded), whatever happened above
+        if (lane == 0) mma_commit(&bar.drain);
+        __syncwarp();
+        mbar_drain(&bar.drain, 0);
     }
 
-    // ---- epilogue: O^T from TMEM; thread = output dim d, N rows
-    const int d = whalf * 128 + quarter * 32 + lane;
-    float o[kRows];
-    {
-        const uint32_t col = whalf ? kColO1 : kColO0;
-#pragma unroll
-        for (int c = 0; c < kRows; c += 8) {
-            if (c < N) {
-                float v8[8];
-                tmem_ld8(tmem + lane_base + col + c, v8);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) o[c + i] = v8[i];
-            }
-        }
-        tmem_ld_wait();
-    }
     if (range_bad && a.status) atomicOr(a.status, Q3KV_STATUS_RANGE);
-    __syncthreads();
-    if (*abort) {
-        // let every copy and MMA this CTA started finish (bounded) before the
-        // shared memory and TMEM are given back
-        if (tid == 0) {
-            mbar_drain(&sm.mma_bar, mma_phase);
-            for (int st = 0; st < 2; ++st)
-                for (int k = waited[st]; k < sm.issued[st]; ++k) mbar_drain(&sm.full_bar[st], (uint32_t)(k & 1));
-        }
-        __syncthreads();
-    }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 12) tmem_dealloc(tmem, kTmemCols);
     if (*abort) {
         if (tid == 0 && a.status) atomicOr(a.status, Q3KV_STATUS_TIMEOUT);
         return;
     }
-
-    const int unit = (slot * a.num_kv_heads + g) * a.row_chunks + chunk;
-    float* outs = reinterpret_cast<float*>(sm.qhi);      // [64][256] floats (Q no longer needed)
     if (n_splits == 1) {
-#pragma unroll
-        for (int r = 0; r < kRows; ++r)
-            if (r < Rc) outs[r * kHeadDim + d] = o[r] / sm.l_run[r];
-    } else {
-        float* po = a.part_o + ((int64_t)unit * a.num_splits + split) * kRows * kHeadDim;
-        float* pml = a.part_ml + ((int64_t)unit * a.num_splits + split) * kRows * 2;
-#pragma unroll
-        for (int r = 0; r < kRows; ++r)
-            if (r < Rc) po[r * kHeadDim + d] = o[r];
-        if (tid < Rc) {
-            pml[2 * tid] = sm.m_run[tid];
-            pml[2 * tid + 1] = sm.l_run[tid];
+        rotate_rows(outs, Rc);
+        for (int idx = tid; idx < Rc * kHeadDim; idx += kThreads) {
+            const int r = idx / kHeadDim, dd = idx % kHeadDim;
+            const int ra = row0 + r;
+            a.out[((q_base + ra / kGroup) * Hq + g * kGroup + ra % kGroup) * kHeadDim + dd] = outs[idx] * 0.0625f;
         }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) sm.flag = (atomicAdd(a.tickets + unit, 1) == n_splits - 1);
-        __syncthreads();
-        if (!sm.flag) return;
-        __threadfence();
-        merge_splits<true>(a.part_o + (int64_t)unit * a.num_splits * kRows * kHeadDim,
-                           a.part_ml + (int64_t)unit * a.num_splits * kRows * 2, n_splits, Rc, kRows,
-                           reinterpret_cast<float*>(sm.vhi), sm.m_run, sm.l_run, outs);
-        if (tid == 0) a.tickets[unit] = 0;
-    }
-    __syncthreads();
-    rotate_rows(outs, Rc);
-    for (int idx = tid; idx < Rc * kHeadDim; idx += kThreads) {
-        const int r = idx / kHeadDim, dd = idx % kHeadDim;
-        const int ra = row0 + r;
-        a.out[((q_base + ra / kGroup) * Hq + g * kGroup + ra % kGroup) * kHeadDim + dd] = outs[idx] * 0.0625f;
     }
 }
 
 }  // namespace
-
-size_t verify_mma_smem_bytes() { return sizeof(MmaSmem); }
 
 cudaError_t launch_verify_mma(const VerifyArgs& a, cudaStream_t stream) {
     const size_t smem = sizeof(MmaSmem);
@@ -746,5 +930,7 @@ cudaError_t launch_verify_mma(const VerifyArgs& a, cudaStream_t stream) {
     }
     return cudaGetLastError();
 }
+
+size_t verify_mma_smem_bytes() { return sizeof(MmaSmem); }
 
 }  // namespace q3kv
