@@ -28,29 +28,37 @@
 //                                        B = P^T in shared memory (MN-major),
 //                                        two 128-dim halves, K = 32 positions
 //
-// Warp roles (13 warps), each tile handed on with mbarriers:
-//   A  warps 0-3   softmax: thread = position; reads S^T from TMEM; scores
-//                  are in log2 units and the running row maximum is only
-//                  raised when a score exceeds it by more than 8 (then l and
-//                  the O^T columns are rescaled), so most tiles need no
-//                  cross-lane maximum; P = 2^(s - m) <= 256 goes to shared
-//                  memory as fp16 hi/lo; row sums by a transposing butterfly.
-//   B1 warps 4-7   K_hat of tile i+1 into TMEM as soon as the QK of tile i has
-//                  read it; also streams the K records (cp.async.bulk, two
-//                  tiles ahead).
-//   B2 warps 8-11  V_hat 32-position sub-tiles into two shared-memory buffers;
-//                  also streams the V records.
-//   M  warp 12     one thread issues every tcgen05.mma (QK of tile i+1 before
-//                  PV of tile i) and commits them to mbarriers.
-// TMEM (512 columns): K_hat hi | K_hat lo | S^T x 2 buffers | O^T x 2 halves.
+// Issue rate, not the tensor pipe, limits small-N MMAs on this GPU: one thread
+// issues a K=16 MMA about every 54 cycles, while an M=128, N=48 MMA executes
+// in about 24.  So four warps issue, each into its own accumulator and each
+// waiting only for its own operands: QK over dims 0..127 into S_a and over
+// 128..255 into S_b (summed by the softmax), PV into the two 128-dim halves of
+// O^T.  Every MMA sequence is fully unrolled, its descriptors formed by
+// constant offsets.
+//
+// Warp roles (16 warps), handing tiles on with mbarriers:
+//   A   warps 0-3   softmax: thread = position; reads S_a + S_b from TMEM;
+//                   scores are in log2 units and the running row maximum is
+//                   only raised when a score exceeds it by more than 8 (then l
+//                   and the O^T columns are rescaled), so most tiles need no
+//                   cross-lane maximum; P = 2^(s - m) <= 256 goes to shared
+//                   memory as fp16 hi/lo; row sums by a transposing butterfly.
+//   B1  warps 4-7   K_hat into TMEM in two halves (dims 0..127, 128..255),
+//                   each as soon as the QK half of the previous tile has read
+//                   it (records prefetched from HBM a tile ahead).
+//   B2  warps 8-11  V_hat 32-position sub-tiles, one shared-memory buffer per
+//                   sub-tile (records prefetched a tile ahead).
+//   MQa, MQb  warps 12-13   one thread each issues a QK half
+//   MP0, MP1  warps 14-15   one thread each issues the PV of an O^T half
+// TMEM (512 columns): K_hat hi | K_hat lo | S_a | S_b | O^T dims 0..127 | 128..255.
 //
 // After the last tile the A warps read O^T (thread = two output dims) and
 // either finish the rows (one split: divide by l, rotate back by H) or store
 // the split partial (m, l, o) for the merge kernel.
 //
 // Every mbarrier wait is bounded (about a second); on a timeout the CTA sets
-// Q3KV_STATUS_TIMEOUT, stops, waits (bounded) for the copies and MMAs it has
-// in flight, frees its TMEM and returns.
+// Q3KV_STATUS_TIMEOUT, stops, waits (bounded) for the MMAs it has in flight,
+// frees its TMEM and returns.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>
@@ -61,12 +69,12 @@
 namespace q3kv {
 namespace {
 
-constexpr int kWarps = 13;
+constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTileP = 128;                 // positions per tile (MMA M of S^T)
 constexpr int kSubP = 32;                   // positions per V sub-tile
+constexpr int kVBufs = 4;                   // one V_hat buffer per sub-tile of a tile
 constexpr int kRows = 64;                   // max query rows per CTA (MMA N <= 64)
-constexpr int kStageBytes = kTileP * kRecordBytes;   // 14,336 B of K (or V) records
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P <= 256
 constexpr long long kWaitCycles = 2000000000LL;
 constexpr float kMaxScale = 18688.0f;       // 3.5 * s must stay below the fp16 maximum
@@ -74,7 +82,8 @@ constexpr float kMaxScale = 18688.0f;       // 3.5 * s must stay below the fp16 
 // TMEM columns (allocation of 512)
 constexpr uint32_t kColKHi = 0;
 constexpr uint32_t kColKLo = 128;
-constexpr uint32_t kColS = 256;             // + 64 * buffer
+constexpr uint32_t kColSa = 256;            // S^T over dims 0..127
+constexpr uint32_t kColSb = 320;            // S^T over dims 128..255
 constexpr uint32_t kColO0 = 384;
 constexpr uint32_t kColO1 = 448;
 constexpr uint32_t kTmemCols = 512;
@@ -83,26 +92,22 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kBarA = 1;                    // the 128 softmax threads
 
 struct Bars {
-    unsigned long long full_k[2], full_v[2];   // records landed (tx bytes)
-    unsigned long long free_k[2], free_v[2];   // records read (4 warps each)
-    unsigned long long kready;                 // K_hat in TMEM (4 warps)
-    unsigned long long qk_done[2];             // S^T buffer written, K_hat read (commit)
-    unsigned long long s_free[2];              // S^T buffer read (4 warps)
-    unsigned long long p_ready;                // P^T stored, O^T rescaled (4 warps)
-    unsigned long long v_ready[4];             // V_hat of sub-tile s filled (1 warp)
-    unsigned long long v_free[4];              // V_hat of sub-tile s read (commit)
-    unsigned long long pv_done;                // all PV of a tile done (commit)
-    unsigned long long drain;                  // everything issued so far done (commit)
+    unsigned long long kready[2];   // K_hat dims half in TMEM (4 B1 warps)
+    unsigned long long qk_done[2];  // S_a / S_b written, that K_hat half read (1 commit)
+    unsigned long long s_free;      // S read (4 A warps)
+    unsigned long long p_ready;     // P^T stored, O^T rescaled (4 A warps)
+    unsigned long long v_ready[4];  // V_hat of sub-tile index q filled (1 warp)
+    unsigned long long v_free[4];   // V_hat of sub-tile index q read (2 commits)
+    unsigned long long pv_done;     // all PV MMAs of a tile done (2 commits)
+    unsigned long long drain[4];    // everything an issuer started is done (1 commit)
 };
 
-struct __align__(1024) MmaSmem {
+struct __align__(16) MmaSmem {
     __half qhi[kRows * kHeadDim];           // B of QK, K-major core layout
     __half qlo[kRows * kHeadDim];
-    __half v[2][2][kSubP * kHeadDim];       // [buffer][hi|lo]: A of PV, MN-major
+    __half v[kVBufs][2][kSubP * kHeadDim];  // [buffer][hi|lo]: A of PV, MN-major
     __half phi[kTileP * kRows];             // B of PV, MN-major
     __half plo[kTileP * kRows];
-    uint8_t stage_k[2][kStageBytes];
-    uint8_t stage_v[2][kStageBytes];
     float m_run[kRows];
     float l_run[kRows];
     float alpha[kRows];
@@ -120,11 +125,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 
 __device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
@@ -161,13 +161,6 @@ __device__ void mbar_drain(unsigned long long* bar, uint32_t parity) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity) && clock64() - t0 <= kWaitCycles) {
     }
-}
-
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, unsigned long long* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -379,21 +372,30 @@ __device__ __forceinline__ bool warp_wait(unsigned long long* bar, uint32_t pari
     return __all_sync(0xffffffffu, ok);
 }
 
-// Page of tile `it` of this split, or -1 if the page table entry is out of range.
+// Page of the tile starting at pos0, or -1 if the page table entry is out of range.
 __device__ __forceinline__ int32_t tile_page(const VerifyArgs& a, const int32_t* pt_row, int pos0) {
     const int32_t page = pt_row[pos0 / kPageSize];
     return (page >= 0 && page < a.num_pages) ? page : -1;
 }
 
-// Load one 112-byte record from shared memory (7 x 16 bytes).
-__device__ __forceinline__ void load_record(const uint8_t* rec, uint32_t (&w)[24], uint32_t (&sc)[4]) {
+// One 112-byte record from the pool (7 x 16-byte loads; a warp reads 32
+// consecutive records, 3,584 contiguous bytes), or zeros.
+__device__ __forceinline__ void fetch_record(const uint8_t* rec, bool valid, uint32_t (&w)[24], uint32_t (&sc)[4]) {
+    if (valid) {
+        const uint4* p = reinterpret_cast<const uint4*>(rec);
 #pragma unroll
-    for (int k = 0; k < 6; ++k) {
-        const uint4 u = reinterpret_cast<const uint4*>(rec)[k];
-        w[4 * k] = u.x; w[4 * k + 1] = u.y; w[4 * k + 2] = u.z; w[4 * k + 3] = u.w;
+        for (int k = 0; k < 6; ++k) {
+            const uint4 u = __ldg(p + k);
+            w[4 * k] = u.x; w[4 * k + 1] = u.y; w[4 * k + 2] = u.z; w[4 * k + 3] = u.w;
+        }
+        const uint4 s = __ldg(p + 6);
+        sc[0] = s.x; sc[1] = s.y; sc[2] = s.z; sc[3] = s.w;
+    } else {
+#pragma unroll
+        for (int k = 0; k < 24; ++k) w[k] = 0u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sc[k] = 0u;
     }
-    const uint4 s = reinterpret_cast<const uint4*>(rec)[6];
-    sc[0] = s.x; sc[1] = s.y; sc[2] = s.z; sc[3] = s.w;
 }
 
 __device__ __forceinline__ __half scale_of(const uint32_t (&sc)[4], int b) {
@@ -445,22 +447,18 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
 
     // ---- set-up: barriers, TMEM, row state, queries
     if (tid == 0) {
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bar.full_k[s], 1);
-            mbar_init(&bar.full_v[s], 1);
-            mbar_init(&bar.free_k[s], 4);
-            mbar_init(&bar.free_v[s], 4);
-            mbar_init(&bar.qk_done[s], 1);
-            mbar_init(&bar.s_free[s], 4);
-        }
+        mbar_init(&bar.kready[0], 4);
+        mbar_init(&bar.kready[1], 4);
+        mbar_init(&bar.qk_done[0], 1);
+        mbar_init(&bar.qk_done[1], 1);
+        mbar_init(&bar.s_free, 4);
+        mbar_init(&bar.p_ready, 4);
         for (int s = 0; s < 4; ++s) {
             mbar_init(&bar.v_ready[s], 1);
-            mbar_init(&bar.v_free[s], 1);
+            mbar_init(&bar.v_free[s], 2);
         }
-        mbar_init(&bar.kready, 4);
-        mbar_init(&bar.p_ready, 4);
-        mbar_init(&bar.pv_done, 1);
-        mbar_init(&bar.drain, 1);
+        mbar_init(&bar.pv_done, 2);
+        for (int k = 0; k < 4; ++k) mbar_init(&bar.drain[k], 1);
         sm.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -529,18 +527,24 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         bool ok = true;
         for (int i = 0; i < n_tiles; ++i) {
-            const int b = i & 1;
-            ok = ok && mbar_wait(&bar.qk_done[b], (uint32_t)((i >> 1) & 1), abort);
+            ok = ok && mbar_wait(&bar.qk_done[0], (uint32_t)(i & 1), abort);
+            ok = ok && mbar_wait(&bar.qk_done[1], (uint32_t)(i & 1), abort);
             tc_fence_after();
             float x[kRows];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                if (16 * c < N) tmem_ld16(tmem + lane_base + kColS + 64 * b + 16 * c, &x[16 * c]);
+                if (16 * c < N) {
+                    float y[16];
+                    tmem_ld16(tmem + lane_base + kColSa + 16 * c, &x[16 * c]);
+                    tmem_ld16(tmem + lane_base + kColSb + 16 * c, y);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) x[16 * c + k] += y[k];
+                }
             }
-            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar.s_free[b]);
+            if (lane == 0) mbar_arrive(&bar.s_free);
 
             const int pos0 = p_begin + i * kTileP;
             const int pos = pos0 + p;
@@ -681,110 +685,73 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         const int q = warp - 4;
         const int p = 32 * q + lane;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        const bool producer = (warp == 4 && lane == 0);
-        int issued = 0, consumed = 0;
-        auto issue = [&](int it) {
-            const int stg = it & 1;
+        auto fetch = [&](int it, uint32_t (&w)[24], uint32_t (&sc)[4]) {
             const int pos0 = p_begin + it * kTileP;
             const int32_t page = tile_page(a, pt_row, pos0);
-            if (page < 0) {
-                if (a.status) atomicOr(a.status, Q3KV_STATUS_BAD_PAGE);
-                mbar_arrive(&bar.full_k[stg]);
-            } else {
-                mbar_arrive_expect_tx(&bar.full_k[stg], kStageBytes);
-                bulk_g2s(sm.stage_k[stg], a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, 0,
-                                                                 pos0 % kPageSize),
-                         kStageBytes, &bar.full_k[stg]);
-            }
+            const bool valid = page >= 0 && pos0 + p < p_end;
+            fetch_record(a.pool + record_offset(a.num_layers, a.num_kv_heads, valid ? page : 0, a.layer, g, 0,
+                                                (pos0 + p) % kPageSize),
+                         valid, w, sc);
+            return valid;
         };
-        if (producer) {
-            issue(0);
-            if (n_tiles > 1) issue(1);
-        }
-        issued = min(n_tiles, 2);
-        for (int i = 0; i < n_tiles; ++i) {
-            const int stg = i & 1;
-            if (!warp_wait(&bar.full_k[stg], (uint32_t)((i >> 1) & 1), abort)) break;
-            consumed = i + 1;
-            if (i > 0 && !warp_wait(&bar.qk_done[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1), abort)) break;
-            tc_fence_after();
-            const int pos0 = p_begin + i * kTileP;
-            const bool valid = tile_page(a, pt_row, pos0) >= 0 && pos0 + p < p_end;
-            uint32_t w[24], sc[4];
-            load_record(sm.stage_k[stg] + p * kRecordBytes, w, sc);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar.free_k[stg]);
+        if (q == 0 && lane == 0)
+            for (int it = 0; it < n_tiles; ++it)
+                if (tile_page(a, pt_row, p_begin + it * kTileP) < 0 && a.status) atomicOr(a.status, Q3KV_STATUS_BAD_PAGE);
+        // one tile: two halves of the dims, each after its QK half of the previous tile
+        auto step = [&](int i, const uint32_t (&w)[24], const uint32_t (&sc)[4], bool valid) -> bool {
 #pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                uint32_t hi[16], lo[16];
-                const __half s = scale_of(sc, b);
-                if (valid) {
-                    dequant_block(&w[3 * b], s, hi, lo);
-                    range_bad |= !(__half2float(s) <= kMaxScale);
-                } else {
+            for (int hh = 0; hh < 2; ++hh) {
+                if (i > 0 && !warp_wait(&bar.qk_done[hh], (uint32_t)((i - 1) & 1), abort)) return false;
+                tc_fence_after();
 #pragma unroll
-                    for (int m = 0; m < 16; ++m) hi[m] = lo[m] = 0u;
+                for (int bb = 0; bb < 4; ++bb) {
+                    const int b = 4 * hh + bb;
+                    uint32_t hi[16], lo[16];
+                    const __half s = scale_of(sc, b);
+                    if (valid) {
+                        dequant_block(&w[3 * b], s, hi, lo);
+                        range_bad |= !(__half2float(s) <= kMaxScale);
+                    } else {
+#pragma unroll
+                        for (int m = 0; m < 16; ++m) hi[m] = lo[m] = 0u;
+                    }
+                    tmem_st16(tmem + lane_base + kColKHi + 16 * b, hi);
+                    tmem_st16(tmem + lane_base + kColKLo + 16 * b, lo);
                 }
-                tmem_st16(tmem + lane_base + kColKHi + 16 * b, hi);
-                tmem_st16(tmem + lane_base + kColKLo + 16 * b, lo);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar.kready);
-            if (warp == 4 && i + 2 < n_tiles) {
-                if (!warp_wait(&bar.free_k[stg], (uint32_t)((i >> 1) & 1), abort)) break;
-                if (producer) issue(i + 2);
-                issued = i + 3;
+                tmem_st_wait();
+                tc_fence_before();
                 __syncwarp();
+                if (lane == 0) mbar_arrive(&bar.kready[hh]);
             }
+            return true;
+        };
+        uint32_t w0[24], s0[4], w1[24], s1[4];
+        bool v0 = fetch(0, w0, s0), v1 = false;
+        for (int i = 0; i < n_tiles; i += 2) {      // ping-pong register sets: no copies
+            if (i + 1 < n_tiles) v1 = fetch(i + 1, w1, s1);
+            if (!step(i, w0, s0, v0)) break;
+            if (i + 1 >= n_tiles) break;
+            if (i + 2 < n_tiles) v0 = fetch(i + 2, w0, s0);
+            if (!step(i + 1, w1, s1, v1)) break;
         }
-        if (producer && *abort)
-            for (int t = consumed; t < issued; ++t) mbar_drain(&bar.full_k[t & 1], (uint32_t)((t >> 1) & 1));
     } else if (warp < 12) {
         // ================================================================ B2: V_hat sub-tiles -> shared memory
         const int q = warp - 8;                      // sub-tile q of every tile
-        const int buf = q & 1;
-        const bool producer = (warp == 8 && lane == 0);
-        int issued = 0, consumed = 0;
-        auto issue = [&](int it) {
-            const int stg = it & 1;
+        const int pt = 32 * q + lane;                // position within the tile
+        auto fetch = [&](int it, uint32_t (&w)[24], uint32_t (&sc)[4]) {
             const int pos0 = p_begin + it * kTileP;
             const int32_t page = tile_page(a, pt_row, pos0);
-            if (page < 0) {
-                mbar_arrive(&bar.full_v[stg]);
-            } else {
-                mbar_arrive_expect_tx(&bar.full_v[stg], kStageBytes);
-                bulk_g2s(sm.stage_v[stg], a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, 1,
-                                                                 pos0 % kPageSize),
-                         kStageBytes, &bar.full_v[stg]);
-            }
+            const bool valid = page >= 0 && pos0 + pt < p_end;
+            fetch_record(a.pool + record_offset(a.num_layers, a.num_kv_heads, valid ? page : 0, a.layer, g, 1,
+                                                (pos0 + pt) % kPageSize),
+                         valid, w, sc);
+            return valid;
         };
-        if (producer) {
-            issue(0);
-            if (n_tiles > 1) issue(1);
-        }
-        issued = min(n_tiles, 2);
-        for (int i = 0; i < n_tiles; ++i) {
-            const int stg = i & 1;
-            if (!warp_wait(&bar.full_v[stg], (uint32_t)((i >> 1) & 1), abort)) break;
-            consumed = i + 1;
-            // buffer q & 1 was last read by PV(i, q - 2) or PV(i - 1, q + 2); each
-            // sub-tile has its own barrier pair, so every waiter sees every phase
-            if (q >= 2) {
-                if (!warp_wait(&bar.v_free[q - 2], (uint32_t)(i & 1), abort)) break;
-            } else if (i >= 1) {
-                if (!warp_wait(&bar.v_free[q + 2], (uint32_t)((i - 1) & 1), abort)) break;
-            }
-            const int pos0 = p_begin + i * kTileP;
-            const int pt = 32 * q + lane;
-            const bool valid = tile_page(a, pt_row, pos0) >= 0 && pos0 + pt < p_end;
-            uint32_t w[24], sc[4];
-            load_record(sm.stage_v[stg] + pt * kRecordBytes, w, sc);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar.free_v[stg]);
-            __half* vh = sm.v[buf][0];
-            __half* vl = sm.v[buf][1];
+        auto step = [&](int i, const uint32_t (&w)[24], const uint32_t (&sc)[4], bool valid) -> bool {
+            // buffer q was last read by the PV of sub-tile q of the previous tile
+            if (i >= 1 && !warp_wait(&bar.v_free[q], (uint32_t)((i - 1) & 1), abort)) return false;
+            __half* vh = sm.v[q][0];
+            __half* vl = sm.v[q][1];
 #pragma unroll
             for (int b = 0; b < 8; ++b) {
                 uint32_t hi[16], lo[16];
@@ -808,83 +775,85 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.v_ready[q]);
-            if (warp == 8 && i + 2 < n_tiles) {
-                if (!warp_wait(&bar.free_v[stg], (uint32_t)((i >> 1) & 1), abort)) break;
-                if (producer) issue(i + 2);
-                issued = i + 3;
-                __syncwarp();
-            }
+            return true;
+        };
+        uint32_t w0[24], s0[4], w1[24], s1[4];
+        bool v0 = fetch(0, w0, s0), v1 = false;
+        for (int i = 0; i < n_tiles; i += 2) {
+            if (i + 1 < n_tiles) v1 = fetch(i + 1, w1, s1);
+            if (!step(i, w0, s0, v0)) break;
+            if (i + 1 >= n_tiles) break;
+            if (i + 2 < n_tiles) v0 = fetch(i + 2, w0, s0);
+            if (!step(i + 1, w1, s1, v1)) break;
         }
-        if (producer && *abort)
-            for (int t = consumed; t < issued; ++t) mbar_drain(&bar.full_v[t & 1], (uint32_t)((t >> 1) & 1));
-    } else {
-        // ================================================================ M: MMA issue
+    } else if (warp < 14) {
+        // ================================================================ MQa / MQb: QK halves
+        const int h = warp - 12;                     // 0: dims 0..127 -> S_a, 1: dims 128..255 -> S_b
         const uint32_t idesc_qk = make_idesc(N, false, false);
+        const uint64_t bq_hi = make_desc(smem_u32(sm.qhi) + h * 8 * 256, kQLbo, kQSbo);
+        const uint64_t bq_lo = make_desc(smem_u32(sm.qlo) + h * 8 * 256, kQLbo, kQSbo);
+        const uint32_t dS = tmem + (h ? kColSb : kColSa);
+        const uint32_t aK_hi = tmem + kColKHi + 64 * h;
+        const uint32_t aK_lo = tmem + kColKLo + 64 * h;
+        for (int i = 0; i < n_tiles; ++i) {
+            if (!warp_wait(&bar.kready[h], (uint32_t)(i & 1), abort)) break;
+            if (i >= 1 && !warp_wait(&bar.s_free, (uint32_t)((i - 1) & 1), abort)) break;
+            tc_fence_after();
+            if (lane == 0) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {   // descriptor start address is in 16-byte units
+                    mma_ts(dS, aK_hi + 8 * j, bq_hi + (uint64_t)(16 * j), idesc_qk, j > 0 ? 1u : 0u);
+                    mma_ts(dS, aK_hi + 8 * j, bq_lo + (uint64_t)(16 * j), idesc_qk, 1u);
+                    mma_ts(dS, aK_lo + 8 * j, bq_hi + (uint64_t)(16 * j), idesc_qk, 1u);
+                }
+                mma_commit(&bar.qk_done[h]);
+            }
+            __syncwarp();
+        }
+        if (lane == 0) mma_commit(&bar.drain[h]);
+        __syncwarp();
+        mbar_drain(&bar.drain[h], 0);
+    } else {
+        // ================================================================ MP0 / MP1: PV halves
+        const int h = warp - 14;                     // O^T dims 128h .. 128h + 127
         const uint32_t idesc_pv = make_idesc(N, true, true);
-        const uint32_t qh = smem_u32(sm.qhi), ql = smem_u32(sm.qlo);
-        const uint32_t ph = smem_u32(sm.phi), pl = smem_u32(sm.plo);
-        for (int i = 0; i <= n_tiles; ++i) {
-            if (i < n_tiles) {
-                const int b = i & 1;
-                if (!warp_wait(&bar.kready, (uint32_t)(i & 1), abort)) break;
-                if (i >= 2 && !warp_wait(&bar.s_free[b], (uint32_t)(((i >> 1) - 1) & 1), abort)) break;
+        const uint32_t dO = tmem + (h ? kColO1 : kColO0);
+        const uint64_t bp_hi = make_desc(smem_u32(sm.phi), kPLbo, kPSbo);
+        const uint64_t bp_lo = make_desc(smem_u32(sm.plo), kPLbo, kPSbo);
+        const uint64_t av_hi0 = make_desc(smem_u32(sm.v[0][0]) + (uint32_t)(16 * h) * kVSbo, kVLbo, kVSbo);
+        const uint64_t av_lo0 = make_desc(smem_u32(sm.v[0][1]) + (uint32_t)(16 * h) * kVSbo, kVLbo, kVSbo);
+        const uint64_t vbuf = (uint64_t)(sizeof(sm.v[0]) >> 4);      // one V buffer, 16-byte units
+        for (int jt = 0; jt < n_tiles; ++jt) {
+            if (!warp_wait(&bar.p_ready, (uint32_t)(jt & 1), abort)) break;
+            bool ok = true;
+#pragma unroll 1
+            for (int s = 0; s < 4; ++s) {
+                ok = warp_wait(&bar.v_ready[s], (uint32_t)(jt & 1), abort);
+                if (!ok) break;
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t dS = tmem + kColS + 64 * b;
-#pragma unroll 1
-                    for (int j = 0; j < 16; ++j) {
-                        const uint64_t bh = make_desc(qh + j * 256, kQLbo, kQSbo);
-                        const uint64_t bl = make_desc(ql + j * 256, kQLbo, kQSbo);
-                        mma_ts(dS, tmem + kColKHi + 8 * j, bh, idesc_qk, j > 0 ? 1u : 0u);
-                        mma_ts(dS, tmem + kColKHi + 8 * j, bl, idesc_qk, 1u);
-                        mma_ts(dS, tmem + kColKLo + 8 * j, bh, idesc_qk, 1u);
+                    const uint64_t bfo = (uint64_t)s * vbuf;
+                    const uint64_t avh = av_hi0 + bfo, avl = av_lo0 + bfo;
+                    const uint64_t bph = bp_hi + (uint64_t)(4 * s * 8);     // (4s) x 128 bytes
+                    const uint64_t bpl = bp_lo + (uint64_t)(4 * s * 8);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const uint32_t acc0 = (jt > 0 || s > 0 || j > 0) ? 1u : 0u;
+                        mma_ss(dO, avh + (uint64_t)(16 * j), bph + (uint64_t)(16 * j), idesc_pv, acc0);
+                        mma_ss(dO, avl + (uint64_t)(16 * j), bph + (uint64_t)(16 * j), idesc_pv, 1u);
+                        mma_ss(dO, avh + (uint64_t)(16 * j), bpl + (uint64_t)(16 * j), idesc_pv, 1u);
                     }
-                    mma_commit(&bar.qk_done[b]);
+                    mma_commit(&bar.v_free[s]);
                 }
                 __syncwarp();
             }
-            if (i >= 1) {
-                const int jt = i - 1;                  // PV of the previous tile
-                if (!warp_wait(&bar.p_ready, (uint32_t)(jt & 1), abort)) break;
-                bool ok = true;
-#pragma unroll 1
-                for (int s = 0; s < 4 && ok; ++s) {
-                    const int vb = s & 1;
-                    ok = warp_wait(&bar.v_ready[s], (uint32_t)(jt & 1), abort);
-                    if (!ok) break;
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t vh = smem_u32(sm.v[vb][0]), vl = smem_u32(sm.v[vb][1]);
-#pragma unroll 1
-                        for (int h = 0; h < 2; ++h) {
-                            const uint32_t dO = tmem + (h ? kColO1 : kColO0);
-#pragma unroll 1
-                            for (int j = 0; j < 2; ++j) {
-                                const uint32_t aoff = (uint32_t)(16 * h) * kVSbo + (uint32_t)(2 * j) * kVLbo;
-                                const uint32_t boff = (uint32_t)(4 * s + 2 * j) * kPLbo;
-                                const uint64_t avh = make_desc(vh + aoff, kVLbo, kVSbo);
-                                const uint64_t avl = make_desc(vl + aoff, kVLbo, kVSbo);
-                                const uint64_t bph = make_desc(ph + boff, kPLbo, kPSbo);
-                                const uint64_t bpl = make_desc(pl + boff, kPLbo, kPSbo);
-                                const uint32_t acc0 = (jt > 0 || s > 0 || j > 0) ? 1u : 0u;
-                                mma_ss(dO, avh, bph, idesc_pv, acc0);
-                                mma_ss(dO, avl, bph, idesc_pv, 1u);
-                                mma_ss(dO, avh, bpl, idesc_pv, 1u);
-                            }
-                        }
-                        mma_commit(&bar.v_free[s]);
-                    }
-                    __syncwarp();
-                }
-                if (!ok) break;
-                if (lane == 0) mma_commit(&bar.pv_done);
-                __syncwarp();
-            }
+            if (!ok) break;
+            if (lane == 0) mma_commit(&bar.pv_done);
+            __syncwarp();
         }
-        // wait for every MMA this thread issued (bounded), whatever happened above
-        if (lane == 0) mma_commit(&bar.drain);
+        if (lane == 0) mma_commit(&bar.drain[2 + h]);
         __syncwarp();
-        mbar_drain(&bar.drain, 0);
+        mbar_drain(&bar.drain[2 + h], 0);
     }
 
     if (range_bad && a.status) atomicOr(a.status, Q3KV_STATUS_RANGE);
