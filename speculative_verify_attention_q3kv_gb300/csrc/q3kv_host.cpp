@@ -75,10 +75,10 @@ int make_plan(const q3kv_cache_desc* d, int32_t num_slots, int64_t max_ctx, int3
         int e = device_sm_count(&sms);
         if (e != Q3KV_OK) return e;
         const int64_t units = std::max<int64_t>(1, (int64_t)num_slots * d->num_kv_heads * p->row_chunks);
-        // FMA leg: about two CTAs per SM.  MMA leg (one CTA per SM): about two
-        // waves, so ragged slots still leave the SMs busy.
-        const int64_t target_ctas = 2 * (int64_t)sms;
-        const int64_t target_splits = std::max<int64_t>(1, (target_ctas + units - 1) / units);
+        // FMA leg: about two CTAs per SM.  Tensor-core leg (one CTA per SM, a
+        // pipeline that takes a few tiles to fill): one wave.
+        const int64_t target_ctas = (impl == Q3KV_IMPL_MMA) ? (int64_t)sms : 2 * (int64_t)sms;
+        const int64_t target_splits = std::max<int64_t>(1, target_ctas / units);
         p->split_pages = (int)std::max<int64_t>(1, (pages + target_splits - 1) / target_splits);
     }
     p->num_splits = (int)((pages + p->split_pages - 1) / p->split_pages);

@@ -1,8 +1,8 @@
 // Split-K merge for both verify legs (the flash-decode combine step).
 //
-// One CTA per (query row, unit) where unit = (slot, kv head, row chunk); the
-// 256 threads own one output dim each.  For a row with partials (m_i, l_i,
-// o_i) from splits i:
+// One CTA per (query row, unit) where unit = (slot, kv head, row chunk); its
+// 256 threads read the partials as float4 over four groups of splits at once.
+// For a row with partials (m_i, l_i, o_i) from splits i:
 //   M = max_i m_i,  w_i = e^(m_i - M) / sum_j e^(m_j - M) l_j,  o = sum_i w_i o_i
 // (base-2 exponentials for the tensor-core leg, whose scores are in log2
 // units), then out = H o / 16 back in the unrotated basis.
@@ -54,7 +54,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(VerifyArgs a, int 
     if (n_splits <= 1 || n_splits > a.num_splits) return;   // single split: the verify kernel wrote the row
 
     const float* pml = a.part_ml + ((int64_t)unit * a.num_splits * rows_per_chunk + r) * 2;
-    const float* po = a.part_o + ((int64_t)unit * a.num_splits * rows_per_chunk + r) * kHeadDim + tid;
     const int64_t ml_stride = (int64_t)rows_per_chunk * 2;
     const int64_t o_stride = (int64_t)rows_per_chunk * kHeadDim;
 
@@ -69,7 +68,11 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(VerifyArgs a, int 
     den = block_reduce(den, false, scratch);
     const float inv = 1.0f / den;
 
-    float acc0 = 0.0f, acc1 = 0.0f, acc2 = 0.0f, acc3 = 0.0f;
+    // thread = (split group sg of 4, dims 4c..4c+3): float4 loads, four groups
+    // of splits in flight at once, combined through shared memory
+    const int sg = tid >> 6, c = tid & 63;
+    const float* po4 = a.part_o + ((int64_t)unit * a.num_splits * rows_per_chunk + r) * kHeadDim + 4 * c;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     for (int i0 = 0; i0 < n_splits; i0 += kWChunk) {
         const int ni = min(kWChunk, n_splits - i0);
         for (int i = tid; i < ni; i += kMergeThreads) {
@@ -77,17 +80,29 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(VerifyArgs a, int 
             w[i] = (mi == -CUDART_INF_F) ? 0.0f : (LOG2 ? exp2f(mi - M) : expf(mi - M)) * inv;
         }
         __syncthreads();
-        int i = 0;
-        for (; i + 4 <= ni; i += 4) {   // four independent loads in flight
-            acc0 = fmaf(w[i], __ldcg(po + (i0 + i) * o_stride), acc0);
-            acc1 = fmaf(w[i + 1], __ldcg(po + (i0 + i + 1) * o_stride), acc1);
-            acc2 = fmaf(w[i + 2], __ldcg(po + (i0 + i + 2) * o_stride), acc2);
-            acc3 = fmaf(w[i + 3], __ldcg(po + (i0 + i + 3) * o_stride), acc3);
+#pragma unroll 4
+        for (int i = sg; i < ni; i += 4) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(po4 + (i0 + i) * o_stride));
+            const float wi = w[i];
+            acc.x = fmaf(wi, v.x, acc.x);
+            acc.y = fmaf(wi, v.y, acc.y);
+            acc.z = fmaf(wi, v.z, acc.z);
+            acc.w = fmaf(wi, v.w, acc.w);
         }
-        for (; i < ni; ++i) acc0 = fmaf(w[i], __ldcg(po + (i0 + i) * o_stride), acc0);
         __syncthreads();
     }
-    row[tid] = (acc0 + acc1) + (acc2 + acc3);
+    float4* part = reinterpret_cast<float4*>(w);     // [4 groups][64 quads]
+    part[sg * 64 + c] = acc;
+    __syncthreads();
+    if (tid < 64) {
+        float4 t = part[tid];
+#pragma unroll
+        for (int k = 1; k < 4; ++k) {
+            const float4 u = part[k * 64 + tid];
+            t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+        }
+        row[4 * tid] = t.x; row[4 * tid + 1] = t.y; row[4 * tid + 2] = t.z; row[4 * tid + 3] = t.w;
+    }
     __syncthreads();
     rotate_rows(row, 1);
     const int ra = row0 + r;

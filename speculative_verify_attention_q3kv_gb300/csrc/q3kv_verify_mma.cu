@@ -77,6 +77,9 @@ constexpr int kVBufs = 4;                   // one V_hat buffer per sub-tile of 
 constexpr int kRows = 64;                   // max query rows per CTA (MMA N <= 64)
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P <= 256
 constexpr long long kWaitCycles = 2000000000LL;
+// A waiting thread is suspended (not spinning) until the phase completes or
+// this many nanoseconds pass, so idle warps leave the issue slots to the others.
+constexpr uint32_t kSuspendHintNs = 100000;
 constexpr float kMaxScale = 18688.0f;       // 3.5 * s must stay below the fp16 maximum
 
 // TMEM columns (allocation of 512)
@@ -135,10 +138,10 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t 
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
