@@ -186,6 +186,33 @@ Q3KV_API int q3kv_verify_attn(void* stream, const q3kv_cache_desc* desc, const v
                      int32_t impl, int32_t split_positions,
                      void* d_workspace, size_t workspace_bytes, int32_t* d_status);
 
+/* ---- verify attention with fixed scratch (no workspace argument) -----------
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot provide a device workspace (another allocator owns all device memory,
+ * a serving loop that must not allocate once running, a binding that only
+ * receives device pointers).  Same arguments and results as q3kv_verify_attn,
+ * minus the workspace: the split-K scratch comes from one array of
+ * Q3KV_NOALLOC_SCRATCH_BYTES in the library's own device memory, which every
+ * GPU that loads the library holds until the process exits.  The call
+ * allocates nothing.
+ *   - A call that needs more scratch than the limit (q3kv_workspace_bytes for
+ *     the same arguments) returns Q3KV_ERR_WORKSPACE_TOO_SMALL and launches
+ *     nothing.
+ *   - The first call on a device looks up the array's device address for that
+ *     device (cudaGetSymbolAddress, with that device current) and caches it;
+ *     make that first call before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (other
+ *     streams, other host threads) race and may return wrong results.  The
+ *     array keeps the last call's contents; the call needs no initial
+ *     contents. */
+#define Q3KV_NOALLOC_SCRATCH_BYTES (16u << 20)
+Q3KV_API int q3kv_verify_attn_noalloc(void* stream, const q3kv_cache_desc* desc, const void* d_pool,
+                     const int32_t* d_page_table, int32_t max_pages_per_slot,
+                     const int32_t* d_ctx_len, const int32_t* d_n_q, const int32_t* d_q_offsets,
+                     int32_t num_slots, int64_t max_ctx_len, int32_t max_n_q, int32_t layer,
+                     const void* q, int32_t dtype, float* out,
+                     int32_t impl, int32_t split_positions, int32_t* d_status);
+
 #ifdef __cplusplus
 }
 #endif

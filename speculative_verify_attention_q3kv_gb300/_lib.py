@@ -65,7 +65,12 @@ PROTOTYPES = {
     "q3kv_verify_attn": (c_int32, [c_void_p, P_desc, c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_void_p,
                                    c_int32, c_int64, c_int32, c_int32, c_void_p, c_int32, c_void_p,
                                    c_int32, c_int32, c_void_p, c_size_t, c_void_p]),
+    "q3kv_verify_attn_noalloc": (c_int32, [c_void_p, P_desc, c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
+                                           c_void_p, c_int32, c_int64, c_int32, c_int32, c_void_p, c_int32,
+                                           c_void_p, c_int32, c_int32, c_void_p]),
 }
+
+Q3KV_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _LIB = None
 

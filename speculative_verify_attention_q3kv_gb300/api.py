@@ -126,3 +126,21 @@ def verify_attn(desc: CacheDesc, pool: torch.Tensor, page_table: torch.Tensor, c
                                       _ptr(out), impl, split_positions, _ptr(workspace),
                                       workspace.numel() * workspace.element_size(), _ptr(status))
     check(rc, "q3kv_verify_attn")
+
+
+def verify_attn_noalloc(desc: CacheDesc, pool: torch.Tensor, page_table: torch.Tensor, ctx_len: torch.Tensor,
+                        n_q: torch.Tensor, q_offsets: torch.Tensor, max_ctx_len: int, max_n_q: int, layer: int,
+                        q: torch.Tensor, out: torch.Tensor, impl: int = _lib.Q3KV_IMPL_AUTO,
+                        split_positions: int = 0, status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """q3kv_verify_attn_noalloc: verify_attn with the library's fixed scratch instead of a workspace.
+
+    For callers that cannot provide device scratch memory; calls that overlap
+    on the GPU share that scratch and must not run concurrently.
+    """
+    if out.dtype != torch.float32:
+        raise TypeError("out must be float32")
+    rc = _lib.load().q3kv_verify_attn_noalloc(_stream(stream), ctypes.byref(desc), _ptr(pool), _ptr(page_table),
+                                              page_table.shape[1], _ptr(ctx_len), _ptr(n_q), _ptr(q_offsets),
+                                              ctx_len.shape[0], max_ctx_len, max_n_q, layer, _ptr(q),
+                                              _dtype_code(q), _ptr(out), impl, split_positions, _ptr(status))
+    check(rc, "q3kv_verify_attn_noalloc")
