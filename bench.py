@@ -36,6 +36,10 @@ import q3kv_inputs as qi  # noqa: E402
 
 METRIC = "verified tokens/s and KV HBM GB/s (fraction of GB300 peak) for 3-bit verify attn"
 FALLBACK_HBM_GBS = 6800.0
+# DRAM bytes (read + write) of one verify-kernel launch, from one ncu capture of
+# this benchmark's launch configuration (profiles/verify_mma_workload2_ctx32768_t6.md);
+# workloads without a capture of the current kernel report null.
+NCU_TRAFFIC_BYTES = {2: 15026688}
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -347,12 +351,14 @@ def run_ours(args, rank, world, local, pg):
         "kv_gbs": kv_bytes * Ly * args.steps / (sum(verify_ms) / 1e3) / 1e9,
         "verify_only_tokens_per_s": tokens_per_step * args.steps / (sum(verify_ms) / 1e3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
-                     "kernel": "q3kv verify (one launch per layer)", "peak_source": peak_kind,
+                     "frac": achieved / peak,
+                     "traffic": NCU_TRAFFIC_BYTES.get(w.key) if args.verify_impl == "auto" else None,
+                     "kernel": "q3kv_verify_attn per layer (verify kernel + split-merge kernel)",
+                     "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": kv_bytes,
                      "mean_launch_us": mean_verify_s * 1e6},
         "clocks": clock_info,
-        "gpu_launches": args.steps * Ly * 2,
+        "gpu_launches": args.steps * Ly * (3 if st.ws.numel() > 0 else 2),
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
