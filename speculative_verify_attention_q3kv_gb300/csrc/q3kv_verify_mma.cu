@@ -26,7 +26,7 @@
 //                                        N = query rows padded to 16, K = 256
 //   O^T[d][r] += V_hat[:][d] . P[:][r]   A = V_hat^T in shared memory (MN-major),
 //                                        B = P^T in shared memory (MN-major),
-//                                        two 128-dim halves, K = 32 positions
+//                                        two 128-dim halves, K = 16 positions
 //
 // Issue rate, not the tensor pipe, limits small-N MMAs on this GPU: one thread
 // issues a K=16 MMA about every 54 cycles, while an M=128, N=48 MMA executes
@@ -36,6 +36,12 @@
 // O^T.  Every MMA sequence is fully unrolled, its descriptors formed by
 // constant offsets.
 //
+// Records reach shared memory by bulk copies (cp.async.bulk, completing on an
+// mbarrier): one 14,336-byte copy per tile for K and one for V (a tile's 128
+// positions are contiguous in a page), two stages each, issued a tile ahead by
+// one thread of the warps that read them.  No warp waits on a global load in
+// the loop, and the dequantising warps hold no prefetch registers.
+//
 // Warp roles (16 warps), handing tiles on with mbarriers:
 //   A   warps 0-3   softmax: thread = position; reads S_a + S_b from TMEM;
 //                   scores are in log2 units and the running row maximum is
@@ -43,11 +49,12 @@
 //                   and the O^T columns are rescaled), so most tiles need no
 //                   cross-lane maximum; P = 2^(s - m) <= 256 goes to shared
 //                   memory as fp16 hi/lo; row sums by a transposing butterfly.
-//   B1  warps 4-7   K_hat into TMEM in two halves (dims 0..127, 128..255),
-//                   each as soon as the QK half of the previous tile has read
-//                   it (records prefetched from HBM a tile ahead).
-//   B2  warps 8-11  V_hat 32-position sub-tiles, one shared-memory buffer per
-//                   sub-tile (records prefetched a tile ahead).
+//   B1  warps 4-7   thread = position: its K record from shared memory, K_hat
+//                   into TMEM in two halves (dims 0..127, 128..255), each as
+//                   soon as the QK half of the previous tile has read it.
+//   B2  warps 8-11  V_hat in 16-position sub-tiles through four shared-memory
+//                   buffers; lane = (position, 32-dim block), all four warps on
+//                   every sub-tile.
 //   MQa, MQb  warps 12-13   one thread each issues a QK half
 //   MP0, MP1  warps 14-15   one thread each issues the PV of an O^T half
 // TMEM (512 columns): K_hat hi | K_hat lo | S_a | S_b | O^T dims 0..127 | 128..255.
@@ -57,8 +64,10 @@
 // the split partial (m, l, o) for the merge kernel.
 //
 // Every mbarrier wait is bounded (about a second); on a timeout the CTA sets
-// Q3KV_STATUS_TIMEOUT, stops, waits (bounded) for the MMAs it has in flight,
-// frees its TMEM and returns.
+// Q3KV_STATUS_TIMEOUT, stops issuing, waits (bounded) for the MMAs and copies
+// it has in flight, frees its TMEM and returns.  Named barriers are only used
+// inside a warp group whose warps all run the same number of iterations, also
+// after a timeout.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>
@@ -72,10 +81,15 @@ namespace {
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTileP = 128;                 // positions per tile (MMA M of S^T)
-constexpr int kSubP = 32;                   // positions per V sub-tile
-constexpr int kVBufs = 4;                   // one V_hat buffer per sub-tile of a tile
+constexpr int kSubP = 16;                   // positions per V sub-tile (one MMA K step)
+constexpr int kSubTiles = kTileP / kSubP;   // 8
+constexpr int kVBufs = 4;                   // V_hat sub-tile ring
+constexpr uint32_t kRecTile = kTileP * kRecordBytes;   // 14,336 bytes of records per tile
 constexpr int kRows = 64;                   // max query rows per CTA (MMA N <= 64)
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P <= 256
+// Initial running maximum: finite, so 2^(s - m) of a masked score (-inf) is 0
+// without a select, and any finite score exceeds it by more than the threshold.
+constexpr float kMInit = -1.0e30f;
 constexpr long long kWaitCycles = 2000000000LL;
 // A waiting thread is suspended (not spinning) until the phase completes or
 // this many nanoseconds pass, so idle warps leave the issue slots to the others.
@@ -93,15 +107,19 @@ constexpr uint32_t kTmemCols = 512;
 
 // named barriers
 constexpr int kBarA = 1;                    // the 128 softmax threads
+constexpr int kBarB1 = 2;                   // the 128 K_hat threads
+constexpr int kBarB2 = 3;                   // the 128 V_hat threads
 
 struct Bars {
+    unsigned long long kfull;       // K records of the next tile landed (bulk copy bytes)
+    unsigned long long vfull;       // V records of the next tile landed
     unsigned long long kready[2];   // K_hat dims half in TMEM (4 B1 warps)
     unsigned long long qk_done[2];  // S_a / S_b written, that K_hat half read (1 commit)
     unsigned long long s_free;      // S read (4 A warps)
-    unsigned long long p_ready;     // P^T stored, O^T rescaled (4 A warps)
-    unsigned long long v_ready[4];  // V_hat of sub-tile index q filled (1 warp)
-    unsigned long long v_free[4];   // V_hat of sub-tile index q read (2 commits)
-    unsigned long long pv_done;     // all PV MMAs of a tile done (2 commits)
+    unsigned long long p_ready[2];  // P^T buffer b stored, O^T rescaled (4 A warps)
+    unsigned long long v_ready[4];  // V_hat buffer b filled (its B2 warp)
+    unsigned long long v_free[4];   // V_hat buffer b read (2 commits)
+    unsigned long long pv_done[2];  // all PV MMAs of a tile with P^T buffer b done (2 commits)
     unsigned long long drain[4];    // everything an issuer started is done (1 commit)
 };
 
@@ -109,9 +127,12 @@ struct __align__(16) MmaSmem {
     __half qhi[kRows * kHeadDim];           // B of QK, K-major core layout
     __half qlo[kRows * kHeadDim];
     __half v[kVBufs][2][kSubP * kHeadDim];  // [buffer][hi|lo]: A of PV, MN-major
-    __half phi[kTileP * kRows];             // B of PV, MN-major
-    __half plo[kTileP * kRows];
+    __half phi[2][kTileP * kRows];          // B of PV, MN-major, double-buffered by tile
+    __half plo[2][kTileP * kRows];
+    uint8_t krec[kRecTile];                 // record stages (bulk copy destinations);
+    uint8_t vrec[kRecTile];                 // their readers copy them to registers first
     float m_run[kRows];
+    float thr[kRows];                       // m_run + threshold
     float l_run[kRows];
     float alpha[kRows];
     int lim[kRows];
@@ -164,6 +185,19 @@ __device__ void mbar_drain(unsigned long long* bar, uint32_t parity) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity) && clock64() - t0 <= kWaitCycles) {
     }
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// Bulk copy global -> shared (16-byte aligned ends, size a multiple of 16),
+// completing `bytes` of transaction count on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, unsigned long long* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -285,12 +319,12 @@ __host__ __device__ constexpr uint32_t make_idesc(int n, bool a_mn_major, bool b
 // ---------------------------------------------------------------- layouts (element offsets)
 // Q (B of QK; N = rows r, K = dims k), K-major: core (r/8, k/8) at ((r/8)*32 + k/8)*64 elements.
 __device__ __forceinline__ int q_off(int r, int k) { return (((r >> 3) * 32 + (k >> 3)) << 6) + ((r & 7) << 3) + (k & 7); }
-// V_hat sub-tile (A of PV; M = dims d, K = positions p < 32), MN-major: core (d/8, p/8).
-__device__ __forceinline__ int v_off(int d, int p) { return (((d >> 3) * 4 + (p >> 3)) << 6) + ((p & 7) << 3) + (d & 7); }
+// V_hat sub-tile (A of PV; M = dims d, K = positions p < 16), MN-major: core (d/8, p/8).
+__device__ __forceinline__ int v_off(int d, int p) { return (((d >> 3) * 2 + (p >> 3)) << 6) + ((p & 7) << 3) + (d & 7); }
 // P^T (B of PV; N = rows r, K = positions p < 128), MN-major: core (r/8, p/8).
 __device__ __forceinline__ int p_off(int r, int p) { return (((r >> 3) * 16 + (p >> 3)) << 6) + ((p & 7) << 3) + (r & 7); }
 constexpr uint32_t kQLbo = 128, kQSbo = 32 * 128;
-constexpr uint32_t kVLbo = 128, kVSbo = 4 * 128;
+constexpr uint32_t kVLbo = 128, kVSbo = 2 * 128;
 constexpr uint32_t kPLbo = 128, kPSbo = 16 * 128;
 
 // ---------------------------------------------------------------- dequantisation
@@ -381,17 +415,17 @@ __device__ __forceinline__ int32_t tile_page(const VerifyArgs& a, const int32_t*
     return (page >= 0 && page < a.num_pages) ? page : -1;
 }
 
-// One 112-byte record from the pool (7 x 16-byte loads; a warp reads 32
-// consecutive records, 3,584 contiguous bytes), or zeros.
-__device__ __forceinline__ void fetch_record(const uint8_t* rec, bool valid, uint32_t (&w)[24], uint32_t (&sc)[4]) {
+// One 112-byte record from a shared-memory stage (7 x 16-byte loads; lanes
+// 112 bytes apart hit eight distinct 16-byte bank groups), or zeros.
+__device__ __forceinline__ void load_record(const uint8_t* rec, bool valid, uint32_t (&w)[24], uint32_t (&sc)[4]) {
     if (valid) {
         const uint4* p = reinterpret_cast<const uint4*>(rec);
 #pragma unroll
         for (int k = 0; k < 6; ++k) {
-            const uint4 u = __ldg(p + k);
+            const uint4 u = p[k];
             w[4 * k] = u.x; w[4 * k + 1] = u.y; w[4 * k + 2] = u.z; w[4 * k + 3] = u.w;
         }
-        const uint4 s = __ldg(p + 6);
+        const uint4 s = p[6];
         sc[0] = s.x; sc[1] = s.y; sc[2] = s.z; sc[3] = s.w;
     } else {
 #pragma unroll
@@ -399,6 +433,23 @@ __device__ __forceinline__ void fetch_record(const uint8_t* rec, bool valid, uin
 #pragma unroll
         for (int k = 0; k < 4; ++k) sc[k] = 0u;
     }
+}
+
+// Issues the bulk copy of one tile's records (kv 0 = K, 1 = V) into a stage,
+// or, for a page id out of range, flags it and completes the stage's phase
+// without data (the readers zero that tile).
+__device__ __forceinline__ void issue_tile_copy(const VerifyArgs& a, const int32_t* pt_row, int g, int kv, int pos0,
+                                                uint8_t* dst, unsigned long long* full) {
+    const int32_t page = pt_row[pos0 / kPageSize];
+    if (page < 0 || page >= a.num_pages) {
+        if (a.status) atomicOr(a.status, Q3KV_STATUS_BAD_PAGE);
+        mbar_arrive(full);
+        return;
+    }
+    const uint8_t* src = a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, kv, pos0 % kPageSize);
+    fence_proxy_async();
+    mbar_arrive_expect_tx(full, kRecTile);
+    bulk_g2s(dst, src, kRecTile, full);
 }
 
 __device__ __forceinline__ __half scale_of(const uint32_t (&sc)[4], int b) {
@@ -448,64 +499,81 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
     volatile int* abort = &sm.abort;
     Bars& bar = sm.bar;
 
-    // ---- set-up: barriers, TMEM, row state, queries
+    // ---- set-up: barriers, first record copies, TMEM, row state, queries
     if (tid == 0) {
-        mbar_init(&bar.kready[0], 4);
-        mbar_init(&bar.kready[1], 4);
-        mbar_init(&bar.qk_done[0], 1);
-        mbar_init(&bar.qk_done[1], 1);
-        mbar_init(&bar.s_free, 4);
-        mbar_init(&bar.p_ready, 4);
-        for (int s = 0; s < 4; ++s) {
-            mbar_init(&bar.v_ready[s], 1);
-            mbar_init(&bar.v_free[s], 2);
+        mbar_init(&bar.kfull, 1);
+        mbar_init(&bar.vfull, 1);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&bar.kready[h], 4);
+            mbar_init(&bar.qk_done[h], 1);
+            mbar_init(&bar.p_ready[h], 4);
+            mbar_init(&bar.pv_done[h], 2);
         }
-        mbar_init(&bar.pv_done, 2);
+        mbar_init(&bar.s_free, 4);
+        for (int b = 0; b < kVBufs; ++b) {
+            mbar_init(&bar.v_ready[b], 1);
+            mbar_init(&bar.v_free[b], 2);
+        }
         for (int k = 0; k < 4; ++k) mbar_init(&bar.drain[k], 1);
         sm.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    __syncthreads();
+    // the first tile's records stream in while the queries are prepared
+    if ((warp == 4 || warp == 8) && lane == 0 && n_tiles > 0) {
+        const int kv = warp == 4 ? 0 : 1;
+        issue_tile_copy(a, pt_row, g, kv, p_begin, kv ? sm.vrec : sm.krec, kv ? &bar.vfull : &bar.kfull);
+    }
     if (warp == 12) tmem_alloc(&sm.tmem_base, kTmemCols);
     if (tid < kRows) {
-        sm.m_run[tid] = -CUDART_INF_F;
+        sm.m_run[tid] = kMInit;
+        sm.thr[tid] = kMInit + kRescaleThreshold;
         sm.l_run[tid] = 0.0f;
         sm.lim[tid] = (tid < Rc) ? min(Nctx + (row0 + tid) / kGroup, p_end - 1) : -1;
     }
-    {   // queries: one warp per row, register butterflies for H, then scale
-        // 1/16 (H) * 1/16 (softmax) * log2(e) and split into fp16 hi + lo
+    {   // queries: one warp per row (four rows per warp, loads first), register
+        // butterflies for H, then scale 1/16 (H) * 1/16 (softmax) * log2(e) and
+        // split into fp16 hi + lo
         const TIn* qin = static_cast<const TIn*>(a.q);
-        for (int r = warp; r < kRows; r += kWarps) {
-            float x[8];
+        constexpr int kRowsPerWarp = kRows / kWarps;
+        float x[kRowsPerWarp][8];
+#pragma unroll
+        for (int k = 0; k < kRowsPerWarp; ++k) {
+            const int r = warp + kWarps * k;
             if (r < Rc) {
                 const int ra = row0 + r;
-                load8(qin + ((q_base + ra / kGroup) * Hq + g * kGroup + ra % kGroup) * kHeadDim + 8 * lane, x);
+                load8(qin + ((q_base + ra / kGroup) * Hq + g * kGroup + ra % kGroup) * kHeadDim + 8 * lane, x[k]);
             } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) x[i] = 0.0f;
+                for (int i = 0; i < 8; ++i) x[k][i] = 0.0f;
             }
+        }
+#pragma unroll
+        for (int k = 0; k < kRowsPerWarp; ++k) {
+            const int r = warp + kWarps * k;
 #pragma unroll
             for (int h = 1; h < 8; h <<= 1)
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
                     if ((i & h) == 0) {
-                        const float lo = x[i], hi = x[i + h];
-                        x[i] = lo + hi;
-                        x[i + h] = lo - hi;
+                        const float lo = x[k][i], hi = x[k][i + h];
+                        x[k][i] = lo + hi;
+                        x[k][i + h] = lo - hi;
                     }
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) {
                 const bool upper = (lane & m) != 0;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
-                    x[i] = upper ? o - x[i] : x[i] + o;
+                    const float o = __shfl_xor_sync(0xffffffffu, x[k][i], m);
+                    x[k][i] = upper ? o - x[k][i] : x[k][i] + o;
                 }
             }
             uint32_t hw[4], lw[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float x0 = x[2 * i] * (1.4426950408889634f / 256.0f);
-                const float x1 = x[2 * i + 1] * (1.4426950408889634f / 256.0f);
+                const float x0 = x[k][2 * i] * (1.4426950408889634f / 256.0f);
+                const float x1 = x[k][2 * i + 1] * (1.4426950408889634f / 256.0f);
                 const __half2 h2 = __floats2half2_rn(x0, x1);
                 const float2 hf = __half22float2(h2);
                 hw[i] = as_u32(h2);
@@ -530,84 +598,94 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         bool ok = true;
         for (int i = 0; i < n_tiles; ++i) {
+            const int pb = i & 1;                       // P^T buffer of this tile
             ok = ok && mbar_wait(&bar.qk_done[0], (uint32_t)(i & 1), abort);
             ok = ok && mbar_wait(&bar.qk_done[1], (uint32_t)(i & 1), abort);
             tc_fence_after();
+            // S = S_a + S_b, 32 columns per TMEM round trip; columns >= N are -inf
             float x[kRows];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (16 * c < N) {
-                    float y[16];
-                    tmem_ld16(tmem + lane_base + kColSa + 16 * c, &x[16 * c]);
-                    tmem_ld16(tmem + lane_base + kColSb + 16 * c, y);
+            for (int c2 = 0; c2 < 2; ++c2) {
+                if (32 * c2 < N) {
+                    float y[32];
+                    tmem_ld16(tmem + lane_base + kColSa + 32 * c2, &x[32 * c2]);
+                    tmem_ld16(tmem + lane_base + kColSb + 32 * c2, &y[0]);
+                    if (32 * c2 + 16 < N) {
+                        tmem_ld16(tmem + lane_base + kColSa + 32 * c2 + 16, &x[32 * c2 + 16]);
+                        tmem_ld16(tmem + lane_base + kColSb + 32 * c2 + 16, &y[16]);
+                    }
                     tmem_ld_wait();
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) x[16 * c + k] += y[k];
+                    for (int k = 0; k < 32; ++k) x[32 * c2 + k] += y[k];
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.s_free);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                if (16 * c >= N)
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) x[16 * c + k] = -CUDART_INF_F;
 
             const int pos0 = p_begin + i * kTileP;
             const int pos = pos0 + p;
             const bool tile_ok = tile_page(a, pt_row, pos0) >= 0;
             const bool interior = tile_ok && pos0 + kTileP - 1 <= min(Nctx, p_end - 1);
+            if (!interior) {   // causal / length mask: row j sees positions <= lim[j]
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const int4 l4 = reinterpret_cast<const int4*>(sm.lim)[c];
+                    const int ll[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (!(tile_ok && pos <= ll[k])) x[4 * c + k] = -CUDART_INF_F;
+                }
+            }
             int over = 0;
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-                const float4 m4 = reinterpret_cast<const float4*>(sm.m_run)[c];
-                const int4 l4 = reinterpret_cast<const int4*>(sm.lim)[c];
-                const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-                const int ll[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int j = 4 * c + k;
-                    float v = x[j];
-                    if (j >= N) v = -CUDART_INF_F;
-                    else if (!interior && !(tile_ok && pos <= ll[k])) v = -CUDART_INF_F;
-                    x[j] = v;
-                    over |= (v > mm[k] + kRescaleThreshold) ? 1 : 0;
-                }
+                const float4 t4 = reinterpret_cast<const float4*>(sm.thr)[c];
+                over |= (x[4 * c] > t4.x) | (x[4 * c + 1] > t4.y) | (x[4 * c + 2] > t4.z) | (x[4 * c + 3] > t4.w);
             }
             const int slow = named_or(kBarA, 128, over);
             if (slow) {
                 // raise the running maxima to cover this tile; rescale l (O below)
+                float t[32];
 #pragma unroll
-                for (int j = 0; j < kRows; ++j) {
-                    if (j < N) {
-                        float mx = x[j];
+                for (int k = 0; k < 32; ++k) t[k] = x[k];
+                sm.red[q][lane] = transpose_reduce<true>(t);
+                if (N > 32) {
 #pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                        if (lane == 0) sm.red[q][j] = mx;
-                    }
+                    for (int k = 0; k < 32; ++k) t[k] = x[32 + k];
+                    sm.red[q][32 + lane] = transpose_reduce<true>(t);
                 }
                 named_sync(kBarA, 128);
                 if (tid < N) {
                     const float mt = fmaxf(fmaxf(sm.red[0][tid], sm.red[1][tid]), fmaxf(sm.red[2][tid], sm.red[3][tid]));
                     const float m_old = sm.m_run[tid];
                     const float m_new = fmaxf(m_old, mt);
-                    const float al = (m_old == -CUDART_INF_F) ? 0.0f : exp2f(m_old - m_new);
+                    const float al = exp2f(m_old - m_new);
                     sm.m_run[tid] = m_new;
+                    sm.thr[tid] = m_new + kRescaleThreshold;
                     sm.l_run[tid] *= al;
                     sm.alpha[tid] = al;
                 }
                 named_sync(kBarA, 128);
             }
-            // P = 2^(s - m) in place
+            // P = 2^(s - m) in place (a masked score gives 0)
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 const float4 m4 = reinterpret_cast<const float4*>(sm.m_run)[c];
-                const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int j = 4 * c + k;
-                    x[j] = (x[j] == -CUDART_INF_F) ? 0.0f : fast_exp2(x[j] - mm[k]);
-                }
+                x[4 * c] = fast_exp2(x[4 * c] - m4.x);
+                x[4 * c + 1] = fast_exp2(x[4 * c + 1] - m4.y);
+                x[4 * c + 2] = fast_exp2(x[4 * c + 2] - m4.z);
+                x[4 * c + 3] = fast_exp2(x[4 * c + 3] - m4.w);
             }
-            // the previous tile's PV must be finished before P^T and O^T change
-            if (i > 0) ok = ok && mbar_wait(&bar.pv_done, (uint32_t)((i - 1) & 1), abort);
+            // P^T buffer pb was last read by the PV of tile i - 2; a rescale of
+            // O^T needs every earlier PV finished (tile i - 1)
             if (slow && i > 0) {
+                ok = ok && mbar_wait(&bar.pv_done[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1), abort);
                 tc_fence_after();
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
@@ -624,7 +702,11 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                     }
                 }
                 tmem_st_wait();
+            } else if (i > 1) {
+                ok = ok && mbar_wait(&bar.pv_done[pb], (uint32_t)(((i - 2) >> 1) & 1), abort);
             }
+            __half* phi = sm.phi[pb];
+            __half* plo = sm.plo[pb];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 if (8 * c < N) {
@@ -637,14 +719,14 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                         h4[k] = as_u32(hh2);
                         l4[k] = as_u32(__floats2half2_rn(a0 - hf.x, a1 - hf.y));
                     }
-                    *reinterpret_cast<uint4*>(&sm.phi[p_off(8 * c, p)]) = make_uint4(h4[0], h4[1], h4[2], h4[3]);
-                    *reinterpret_cast<uint4*>(&sm.plo[p_off(8 * c, p)]) = make_uint4(l4[0], l4[1], l4[2], l4[3]);
+                    *reinterpret_cast<uint4*>(&phi[p_off(8 * c, p)]) = make_uint4(h4[0], h4[1], h4[2], h4[3]);
+                    *reinterpret_cast<uint4*>(&plo[p_off(8 * c, p)]) = make_uint4(l4[0], l4[1], l4[2], l4[3]);
                 }
             }
             fence_proxy_async();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar.p_ready);
+            if (lane == 0) mbar_arrive(&bar.p_ready[pb]);
             // row sums of this tile
             sm.red[q][lane] = transpose_reduce<false>(*reinterpret_cast<float(*)[32]>(&x[0]));
             if (N > 32) sm.red[q][32 + lane] = transpose_reduce<false>(*reinterpret_cast<float(*)[32]>(&x[32]));
@@ -653,7 +735,7 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         }
         named_sync(kBarA, 128);   // l_run complete
         // ---- epilogue: O^T -> partial or finished rows
-        ok = ok && mbar_wait(&bar.pv_done, (uint32_t)((n_tiles - 1) & 1), abort);
+        if (n_tiles > 0) ok = ok && mbar_wait(&bar.pv_done[(n_tiles - 1) & 1], (uint32_t)(((n_tiles - 1) >> 1) & 1), abort);
         tc_fence_after();
         if (ok) {
             const int unit = (slot * a.num_kv_heads + g) * a.row_chunks + chunk;
@@ -688,36 +770,33 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         const int q = warp - 4;
         const int p = 32 * q + lane;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        auto fetch = [&](int it, uint32_t (&w)[24], uint32_t (&sc)[4]) {
-            const int pos0 = p_begin + it * kTileP;
-            const int32_t page = tile_page(a, pt_row, pos0);
-            const bool valid = page >= 0 && pos0 + p < p_end;
-            fetch_record(a.pool + record_offset(a.num_layers, a.num_kv_heads, valid ? page : 0, a.layer, g, 0,
-                                                (pos0 + p) % kPageSize),
-                         valid, w, sc);
-            return valid;
-        };
-        if (q == 0 && lane == 0)
-            for (int it = 0; it < n_tiles; ++it)
-                if (tile_page(a, pt_row, p_begin + it * kTileP) < 0 && a.status) atomicOr(a.status, Q3KV_STATUS_BAD_PAGE);
-        // one tile: two halves of the dims, each after its QK half of the previous tile
-        auto step = [&](int i, const uint32_t (&w)[24], const uint32_t (&sc)[4], bool valid) -> bool {
+        const bool producer = (q == 0 && lane == 0);
+        int pend = n_tiles > 0 ? 0 : -1;             // tile whose copy is issued, not yet seen by the producer
+        bool ok = true;
+        for (int i = 0; i < n_tiles; ++i) {
+            ok = ok && warp_wait(&bar.kfull, (uint32_t)(i & 1), abort);
+            if (producer && ok) pend = -1;
+            const int pos0 = p_begin + i * kTileP;
+            const bool valid = ok && tile_page(a, pt_row, pos0) >= 0 && pos0 + p < p_end;
+            uint32_t w[24], sc[4];
+            load_record(sm.krec + kRecordBytes * p, valid, w, sc);
+            named_sync(kBarB1, 128);   // the stage is read: refill it with tile i + 1
+            if (producer && ok && i + 1 < n_tiles && !*abort) {
+                issue_tile_copy(a, pt_row, g, 0, pos0 + kTileP, sm.krec, &bar.kfull);
+                pend = i + 1;
+            }
+            // two halves of the dims, each after its QK half of the previous tile
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                if (i > 0 && !warp_wait(&bar.qk_done[hh], (uint32_t)((i - 1) & 1), abort)) return false;
+                if (i > 0) ok = ok && warp_wait(&bar.qk_done[hh], (uint32_t)((i - 1) & 1), abort);
                 tc_fence_after();
 #pragma unroll
                 for (int bb = 0; bb < 4; ++bb) {
                     const int b = 4 * hh + bb;
                     uint32_t hi[16], lo[16];
                     const __half s = scale_of(sc, b);
-                    if (valid) {
-                        dequant_block(&w[3 * b], s, hi, lo);
-                        range_bad |= !(__half2float(s) <= kMaxScale);
-                    } else {
-#pragma unroll
-                        for (int m = 0; m < 16; ++m) hi[m] = lo[m] = 0u;
-                    }
+                    dequant_block(&w[3 * b], s, hi, lo);
+                    range_bad |= valid && !(__half2float(s) <= kMaxScale);
                     tmem_st16(tmem + lane_base + kColKHi + 16 * b, hi);
                     tmem_st16(tmem + lane_base + kColKLo + 16 * b, lo);
                 }
@@ -726,69 +805,77 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar.kready[hh]);
             }
-            return true;
-        };
-        uint32_t w0[24], s0[4], w1[24], s1[4];
-        bool v0 = fetch(0, w0, s0), v1 = false;
-        for (int i = 0; i < n_tiles; i += 2) {      // ping-pong register sets: no copies
-            if (i + 1 < n_tiles) v1 = fetch(i + 1, w1, s1);
-            if (!step(i, w0, s0, v0)) break;
-            if (i + 1 >= n_tiles) break;
-            if (i + 2 < n_tiles) v0 = fetch(i + 2, w0, s0);
-            if (!step(i + 1, w1, s1, v1)) break;
         }
+        // after a timeout: wait (bounded) for a copy still landing in shared memory
+        if (producer && pend >= 0) mbar_drain(&bar.kfull, (uint32_t)(pend & 1));
     } else if (warp < 12) {
         // ================================================================ B2: V_hat sub-tiles -> shared memory
-        const int q = warp - 8;                      // sub-tile q of every tile
-        const int pt = 32 * q + lane;                // position within the tile
-        auto fetch = [&](int it, uint32_t (&w)[24], uint32_t (&sc)[4]) {
-            const int pos0 = p_begin + it * kTileP;
-            const int32_t page = tile_page(a, pt_row, pos0);
-            const bool valid = page >= 0 && pos0 + pt < p_end;
-            fetch_record(a.pool + record_offset(a.num_layers, a.num_kv_heads, valid ? page : 0, a.layer, g, 1,
-                                                (pos0 + pt) % kPageSize),
-                         valid, w, sc);
-            return valid;
-        };
-        auto step = [&](int i, const uint32_t (&w)[24], const uint32_t (&sc)[4], bool valid) -> bool {
-            // buffer q was last read by the PV of sub-tile q of the previous tile
-            if (i >= 1 && !warp_wait(&bar.v_free[q], (uint32_t)((i - 1) & 1), abort)) return false;
-            __half* vh = sm.v[q][0];
-            __half* vl = sm.v[q][1];
+        // Warp q fills ring buffer q with sub-tiles q and q + 4 of every tile.
+        // Its 256 (position, 32-dim block) items of a tile are read from the
+        // record stage into registers at the start of the tile, 8 per lane:
+        // item j of sub-tile half e covers position 8 (j >> 1) + (lane & 7) and
+        // block 4 (j & 1) + (lane >> 3) of sub-tile q + 4e.
+        const int q = warp - 8;
+        const bool producer = (q == 0 && lane == 0);
+        int pend = n_tiles > 0 ? 0 : -1;
+        bool ok = true;
+        for (int i = 0; i < n_tiles; ++i) {
+            ok = ok && warp_wait(&bar.vfull, (uint32_t)(i & 1), abort);
+            if (producer && ok) pend = -1;
+            const int pos0 = p_begin + i * kTileP;
+            const bool tile_ok = ok && tile_page(a, pt_row, pos0) >= 0;
+            uint32_t w[2][4][3];
+            uint32_t sh[2][4];
 #pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                uint32_t hi[16], lo[16];
-                const __half s = scale_of(sc, b);
-                if (valid) {
-                    dequant_block(&w[3 * b], s, hi, lo);
-                    range_bad |= !(__half2float(s) <= kMaxScale);
-                } else {
+            for (int e = 0; e < 2; ++e)
 #pragma unroll
-                    for (int m = 0; m < 16; ++m) hi[m] = lo[m] = 0u;
+                for (int j = 0; j < 4; ++j) {
+                    const int pt = kSubP * (q + 4 * e) + 8 * (j >> 1) + (lane & 7);
+                    const int blk = 4 * (j & 1) + (lane >> 3);
+                    if (tile_ok && pos0 + pt < p_end) {
+                        const uint8_t* r = sm.vrec + kRecordBytes * pt;
+                        const uint32_t* wp = reinterpret_cast<const uint32_t*>(r + 12 * blk);
+                        w[e][j][0] = wp[0]; w[e][j][1] = wp[1]; w[e][j][2] = wp[2];
+                        sh[e][j] = *reinterpret_cast<const unsigned short*>(r + 96 + 2 * blk);
+                    } else {
+                        w[e][j][0] = w[e][j][1] = w[e][j][2] = 0u;
+                        sh[e][j] = 0u;
+                    }
                 }
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int d0 = 32 * b + 8 * c;
-                    *reinterpret_cast<uint4*>(&vh[v_off(d0, lane)]) =
-                        make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
-                    *reinterpret_cast<uint4*>(&vl[v_off(d0, lane)]) =
-                        make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
-                }
+            named_sync(kBarB2, 128);   // the stage is read: refill it with tile i + 1
+            if (producer && ok && i + 1 < n_tiles && !*abort) {
+                issue_tile_copy(a, pt_row, g, 1, pos0 + kTileP, sm.vrec, &bar.vfull);
+                pend = i + 1;
             }
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar.v_ready[q]);
-            return true;
-        };
-        uint32_t w0[24], s0[4], w1[24], s1[4];
-        bool v0 = fetch(0, w0, s0), v1 = false;
-        for (int i = 0; i < n_tiles; i += 2) {
-            if (i + 1 < n_tiles) v1 = fetch(i + 1, w1, s1);
-            if (!step(i, w0, s0, v0)) break;
-            if (i + 1 >= n_tiles) break;
-            if (i + 2 < n_tiles) v0 = fetch(i + 2, w0, s0);
-            if (!step(i + 1, w1, s1, v1)) break;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int k = 2 * i + e;                 // use of buffer q
+                if (k >= 1) ok = ok && warp_wait(&bar.v_free[q], (uint32_t)((k - 1) & 1), abort);
+                __half* vh = sm.v[q][0];
+                __half* vl = sm.v[q][1];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int pl = 8 * (j >> 1) + (lane & 7);
+                    const int blk = 4 * (j & 1) + (lane >> 3);
+                    uint32_t hi[16], lo[16];
+                    const __half s = __ushort_as_half((unsigned short)sh[e][j]);
+                    dequant_block(w[e][j], s, hi, lo);
+                    range_bad |= !(__half2float(s) <= kMaxScale);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int d0 = 32 * blk + 8 * c;
+                        *reinterpret_cast<uint4*>(&vh[v_off(d0, pl)]) =
+                            make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+                        *reinterpret_cast<uint4*>(&vl[v_off(d0, pl)]) =
+                            make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+                    }
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar.v_ready[q]);
+            }
         }
+        if (producer && pend >= 0) mbar_drain(&bar.vfull, (uint32_t)(pend & 1));
     } else if (warp < 14) {
         // ================================================================ MQa / MQb: QK halves
         const int h = warp - 12;                     // 0: dims 0..127 -> S_a, 1: dims 128..255 -> S_b
@@ -821,37 +908,36 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         const int h = warp - 14;                     // O^T dims 128h .. 128h + 127
         const uint32_t idesc_pv = make_idesc(N, true, true);
         const uint32_t dO = tmem + (h ? kColO1 : kColO0);
-        const uint64_t bp_hi = make_desc(smem_u32(sm.phi), kPLbo, kPSbo);
-        const uint64_t bp_lo = make_desc(smem_u32(sm.plo), kPLbo, kPSbo);
+        const uint64_t bp_hi0 = make_desc(smem_u32(sm.phi[0]), kPLbo, kPSbo);
+        const uint64_t bp_lo0 = make_desc(smem_u32(sm.plo[0]), kPLbo, kPSbo);
+        const uint64_t pbuf = (uint64_t)(sizeof(sm.phi[0]) >> 4);    // one P^T buffer, 16-byte units
         const uint64_t av_hi0 = make_desc(smem_u32(sm.v[0][0]) + (uint32_t)(16 * h) * kVSbo, kVLbo, kVSbo);
         const uint64_t av_lo0 = make_desc(smem_u32(sm.v[0][1]) + (uint32_t)(16 * h) * kVSbo, kVLbo, kVSbo);
         const uint64_t vbuf = (uint64_t)(sizeof(sm.v[0]) >> 4);      // one V buffer, 16-byte units
         for (int jt = 0; jt < n_tiles; ++jt) {
-            if (!warp_wait(&bar.p_ready, (uint32_t)(jt & 1), abort)) break;
+            const int pb = jt & 1;
+            if (!warp_wait(&bar.p_ready[pb], (uint32_t)((jt >> 1) & 1), abort)) break;
             bool ok = true;
 #pragma unroll 1
-            for (int s = 0; s < 4; ++s) {
-                ok = warp_wait(&bar.v_ready[s], (uint32_t)(jt & 1), abort);
+            for (int sub = 0; sub < kSubTiles; ++sub) {
+                // sub-tile sub sits in buffer sub % 4, that buffer's use 2 jt + sub / 4
+                const int b = sub & (kVBufs - 1);
+                ok = warp_wait(&bar.v_ready[b], (uint32_t)((2 * jt + sub / kVBufs) & 1), abort);
                 if (!ok) break;
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint64_t bfo = (uint64_t)s * vbuf;
-                    const uint64_t avh = av_hi0 + bfo, avl = av_lo0 + bfo;
-                    const uint64_t bph = bp_hi + (uint64_t)(4 * s * 8);     // (4s) x 128 bytes
-                    const uint64_t bpl = bp_lo + (uint64_t)(4 * s * 8);
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const uint32_t acc0 = (jt > 0 || s > 0 || j > 0) ? 1u : 0u;
-                        mma_ss(dO, avh + (uint64_t)(16 * j), bph + (uint64_t)(16 * j), idesc_pv, acc0);
-                        mma_ss(dO, avl + (uint64_t)(16 * j), bph + (uint64_t)(16 * j), idesc_pv, 1u);
-                        mma_ss(dO, avh + (uint64_t)(16 * j), bpl + (uint64_t)(16 * j), idesc_pv, 1u);
-                    }
-                    mma_commit(&bar.v_free[s]);
+                    const uint64_t bfo = (uint64_t)b * vbuf;
+                    const uint64_t koff = (uint64_t)pb * pbuf + (uint64_t)(16 * sub);   // 2 sub x 128 bytes along K
+                    const uint32_t acc0 = (jt > 0 || sub > 0) ? 1u : 0u;
+                    mma_ss(dO, av_hi0 + bfo, bp_hi0 + koff, idesc_pv, acc0);
+                    mma_ss(dO, av_lo0 + bfo, bp_hi0 + koff, idesc_pv, 1u);
+                    mma_ss(dO, av_hi0 + bfo, bp_lo0 + koff, idesc_pv, 1u);
+                    mma_commit(&bar.v_free[b]);
                 }
                 __syncwarp();
             }
             if (!ok) break;
-            if (lane == 0) mma_commit(&bar.pv_done);
+            if (lane == 0) mma_commit(&bar.pv_done[pb]);
             __syncwarp();
         }
         if (lane == 0) mma_commit(&bar.drain[2 + h]);
