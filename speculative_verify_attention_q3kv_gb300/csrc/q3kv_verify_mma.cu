@@ -107,12 +107,10 @@ constexpr uint32_t kTmemCols = 512;
 
 // named barriers
 constexpr int kBarA = 1;                    // the 128 softmax threads
-constexpr int kBarB1 = 2;                   // the 128 K_hat threads
-constexpr int kBarB2 = 3;                   // the 128 V_hat threads
 
 struct Bars {
-    unsigned long long kfull;       // K records of the next tile landed (bulk copy bytes)
-    unsigned long long vfull;       // V records of the next tile landed
+    unsigned long long kfull[4];    // K records of B1 warp q's 32 positions landed (bulk copy bytes)
+    unsigned long long vfull[4][2]; // V records of B2 warp q's sub-tile q + 4e landed
     unsigned long long kready[2];   // K_hat dims half in TMEM (4 B1 warps)
     unsigned long long qk_done[2];  // S_a / S_b written, that K_hat half read (1 commit)
     unsigned long long s_free;      // S read (4 A warps)
@@ -135,7 +133,6 @@ struct __align__(16) MmaSmem {
     float thr[kRows];                       // m_run + threshold
     float l_run[kRows];
     float alpha[kRows];
-    int lim[kRows];
     float red[4][kRows];
     Bars bar;
     uint32_t tmem_base;
@@ -435,21 +432,23 @@ __device__ __forceinline__ void load_record(const uint8_t* rec, bool valid, uint
     }
 }
 
-// Issues the bulk copy of one tile's records (kv 0 = K, 1 = V) into a stage,
-// or, for a page id out of range, flags it and completes the stage's phase
-// without data (the readers zero that tile).
-__device__ __forceinline__ void issue_tile_copy(const VerifyArgs& a, const int32_t* pt_row, int g, int kv, int pos0,
-                                                uint8_t* dst, unsigned long long* full) {
+// Issues the bulk copy of n records (kv 0 = K, 1 = V) of the tile at pos0,
+// starting at row r0 of the tile, or, for a page id out of range, flags it
+// and completes the phase without data (the readers zero that tile).
+__device__ __forceinline__ void issue_rec_copy(const VerifyArgs& a, const int32_t* pt_row, int g, int kv, int pos0,
+                                               int r0, int n, uint8_t* dst, unsigned long long* full) {
     const int32_t page = pt_row[pos0 / kPageSize];
     if (page < 0 || page >= a.num_pages) {
         if (a.status) atomicOr(a.status, Q3KV_STATUS_BAD_PAGE);
         mbar_arrive(full);
         return;
     }
-    const uint8_t* src = a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, kv, pos0 % kPageSize);
+    const uint8_t* src =
+        a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, kv, pos0 % kPageSize + r0);
+    const uint32_t bytes = (uint32_t)(n * kRecordBytes);
     fence_proxy_async();
-    mbar_arrive_expect_tx(full, kRecTile);
-    bulk_g2s(dst, src, kRecTile, full);
+    mbar_arrive_expect_tx(full, bytes);
+    bulk_g2s(dst, src, bytes, full);
 }
 
 __device__ __forceinline__ __half scale_of(const uint32_t (&sc)[4], int b) {
@@ -501,8 +500,11 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
 
     // ---- set-up: barriers, first record copies, TMEM, row state, queries
     if (tid == 0) {
-        mbar_init(&bar.kfull, 1);
-        mbar_init(&bar.vfull, 1);
+        for (int q = 0; q < 4; ++q) {
+            mbar_init(&bar.kfull[q], 1);
+            mbar_init(&bar.vfull[q][0], 1);
+            mbar_init(&bar.vfull[q][1], 1);
+        }
         for (int h = 0; h < 2; ++h) {
             mbar_init(&bar.kready[h], 4);
             mbar_init(&bar.qk_done[h], 1);
@@ -519,17 +521,26 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    // the first tile's records stream in while the queries are prepared
-    if ((warp == 4 || warp == 8) && lane == 0 && n_tiles > 0) {
-        const int kv = warp == 4 ? 0 : 1;
-        issue_tile_copy(a, pt_row, g, kv, p_begin, kv ? sm.vrec : sm.krec, kv ? &bar.vfull : &bar.kfull);
+    // the first tile's records stream in while the queries are prepared:
+    // each dequantising warp copies its own positions
+    if (warp >= 4 && warp < 12 && lane == 0 && n_tiles > 0) {
+        const int q = warp & 3;
+        if (warp < 8) {
+            issue_rec_copy(a, pt_row, g, 0, p_begin, 32 * q, 32, sm.krec + kRecordBytes * 32 * q, &bar.kfull[q]);
+        } else {
+            for (int e = 0; e < 2; ++e) {
+                const int r0 = kSubP * (q + 4 * e);
+                issue_rec_copy(a, pt_row, g, 1, p_begin, r0, kSubP, sm.vrec + kRecordBytes * r0, &bar.vfull[q][e]);
+            }
+        }
     }
     if (warp == 12) tmem_alloc(&sm.tmem_base, kTmemCols);
     if (tid < kRows) {
-        sm.m_run[tid] = kMInit;
-        sm.thr[tid] = kMInit + kRescaleThreshold;
+        // padding rows (>= Rc) get a running maximum of 0 and a threshold no
+        // score exceeds: they never trigger a rescale and are never stored
+        sm.m_run[tid] = (tid < Rc) ? kMInit : 0.0f;
+        sm.thr[tid] = (tid < Rc) ? kMInit + kRescaleThreshold : CUDART_INF_F;
         sm.l_run[tid] = 0.0f;
-        sm.lim[tid] = (tid < Rc) ? min(Nctx + (row0 + tid) / kGroup, p_end - 1) : -1;
     }
     {   // queries: one warp per row (four rows per warp, loads first), register
         // butterflies for H, then scale 1/16 (H) * 1/16 (softmax) * log2(e) and
@@ -632,15 +643,14 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
             const int pos = pos0 + p;
             const bool tile_ok = tile_page(a, pt_row, pos0) >= 0;
             const bool interior = tile_ok && pos0 + kTileP - 1 <= min(Nctx, p_end - 1);
-            if (!interior) {   // causal / length mask: row j sees positions <= lim[j]
+            if (!interior) {
+                // causal / length mask.  Row r (token (row0 + r) / 8) sees
+                // positions <= Nctx + (row0 + r) / 8, so position pos is seen by
+                // rows r >= 8 (pos - Nctx) - row0; nothing past p_end is seen.
+                const int r_min = (tile_ok && pos < p_end) ? max(0, kGroup * (pos - Nctx) - row0) : kRows;
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const int4 l4 = reinterpret_cast<const int4*>(sm.lim)[c];
-                    const int ll[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        if (!(tile_ok && pos <= ll[k])) x[4 * c + k] = -CUDART_INF_F;
-                }
+                for (int j = 0; j < kRows; ++j)
+                    if (j < r_min) x[j] = -CUDART_INF_F;
             }
             int over = 0;
 #pragma unroll
@@ -651,17 +661,17 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
             const int slow = named_or(kBarA, 128, over);
             if (slow) {
                 // raise the running maxima to cover this tile; rescale l (O below)
-                float t[32];
+#pragma unroll 1
+                for (int c = 0; c < 2; ++c) {
+                    if (32 * c < N) {
+                        float t[32];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) t[k] = x[k];
-                sm.red[q][lane] = transpose_reduce<true>(t);
-                if (N > 32) {
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) t[k] = x[32 + k];
-                    sm.red[q][32 + lane] = transpose_reduce<true>(t);
+                        for (int k = 0; k < 32; ++k) t[k] = c ? x[32 + k] : x[k];
+                        sm.red[q][32 * c + lane] = transpose_reduce<true>(t);
+                    }
                 }
                 named_sync(kBarA, 128);
-                if (tid < N) {
+                if (tid < Rc) {
                     const float mt = fmaxf(fmaxf(sm.red[0][tid], sm.red[1][tid]), fmaxf(sm.red[2][tid], sm.red[3][tid]));
                     const float m_old = sm.m_run[tid];
                     const float m_new = fmaxf(m_old, mt);
@@ -770,35 +780,52 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         const int q = warp - 4;
         const int p = 32 * q + lane;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        const bool producer = (q == 0 && lane == 0);
+        const bool producer = (lane == 0);           // each B1 warp copies its own 32 records
         int pend = n_tiles > 0 ? 0 : -1;             // tile whose copy is issued, not yet seen by the producer
         bool ok = true;
         for (int i = 0; i < n_tiles; ++i) {
-            ok = ok && warp_wait(&bar.kfull, (uint32_t)(i & 1), abort);
+            ok = ok && warp_wait(&bar.kfull[q], (uint32_t)(i & 1), abort);
             if (producer && ok) pend = -1;
             const int pos0 = p_begin + i * kTileP;
             const bool valid = ok && tile_page(a, pt_row, pos0) >= 0 && pos0 + p < p_end;
-            uint32_t w[24], sc[4];
-            load_record(sm.krec + kRecordBytes * p, valid, w, sc);
-            named_sync(kBarB1, 128);   // the stage is read: refill it with tile i + 1
-            if (producer && ok && i + 1 < n_tiles && !*abort) {
-                issue_tile_copy(a, pt_row, g, 0, pos0 + kTileP, sm.krec, &bar.kfull);
-                pend = i + 1;
-            }
+            const uint8_t* rec = sm.krec + kRecordBytes * p;
             // two halves of the dims, each after its QK half of the previous tile
-#pragma unroll
+#pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
+                uint32_t w[12], sc[2];
+                if (valid) {
+                    const uint4* r4 = reinterpret_cast<const uint4*>(rec + 48 * hh);
+#pragma unroll
+                    for (int m = 0; m < 3; ++m) {
+                        const uint4 u = r4[m];
+                        w[4 * m] = u.x; w[4 * m + 1] = u.y; w[4 * m + 2] = u.z; w[4 * m + 3] = u.w;
+                    }
+                    const uint2 s2 = *reinterpret_cast<const uint2*>(rec + 96 + 8 * hh);
+                    sc[0] = s2.x; sc[1] = s2.y;
+                } else {
+#pragma unroll
+                    for (int m = 0; m < 12; ++m) w[m] = 0u;
+                    sc[0] = sc[1] = 0u;
+                }
+                if (hh == 1) {
+                    __syncwarp();   // this warp's records are read: refill them with tile i + 1
+                    if (producer && ok && i + 1 < n_tiles && !*abort) {
+                        issue_rec_copy(a, pt_row, g, 0, pos0 + kTileP, 32 * q, 32, sm.krec + kRecordBytes * 32 * q,
+                                       &bar.kfull[q]);
+                        pend = i + 1;
+                    }
+                }
                 if (i > 0) ok = ok && warp_wait(&bar.qk_done[hh], (uint32_t)((i - 1) & 1), abort);
                 tc_fence_after();
+                const uint32_t col = tmem + lane_base + 64 * hh;
 #pragma unroll
                 for (int bb = 0; bb < 4; ++bb) {
-                    const int b = 4 * hh + bb;
                     uint32_t hi[16], lo[16];
-                    const __half s = scale_of(sc, b);
-                    dequant_block(&w[3 * b], s, hi, lo);
+                    const __half s = __ushort_as_half((unsigned short)((bb & 1) ? (sc[bb >> 1] >> 16) : (sc[bb >> 1] & 0xFFFFu)));
+                    dequant_block(&w[3 * bb], s, hi, lo);
                     range_bad |= valid && !(__half2float(s) <= kMaxScale);
-                    tmem_st16(tmem + lane_base + kColKHi + 16 * b, hi);
-                    tmem_st16(tmem + lane_base + kColKLo + 16 * b, lo);
+                    tmem_st16(col + kColKHi + 16 * bb, hi);
+                    tmem_st16(col + kColKLo + 16 * bb, lo);
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -807,60 +834,46 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
             }
         }
         // after a timeout: wait (bounded) for a copy still landing in shared memory
-        if (producer && pend >= 0) mbar_drain(&bar.kfull, (uint32_t)(pend & 1));
+        if (producer && pend >= 0) mbar_drain(&bar.kfull[q], (uint32_t)(pend & 1));
     } else if (warp < 12) {
         // ================================================================ B2: V_hat sub-tiles -> shared memory
-        // Warp q fills ring buffer q with sub-tiles q and q + 4 of every tile.
-        // Its 256 (position, 32-dim block) items of a tile are read from the
-        // record stage into registers at the start of the tile, 8 per lane:
-        // item j of sub-tile half e covers position 8 (j >> 1) + (lane & 7) and
-        // block 4 (j & 1) + (lane >> 3) of sub-tile q + 4e.
+        // Warp q fills ring buffer q with sub-tiles q and q + 4 of every tile,
+        // from its own two 16-record copies.  Lane = (position pl, 32-dim block
+        // blk); item j covers pl = 8 (j >> 1) + (lane & 7), blk = 4 (j & 1) + (lane >> 3).
         const int q = warp - 8;
-        const bool producer = (q == 0 && lane == 0);
-        int pend = n_tiles > 0 ? 0 : -1;
+        const bool producer = (lane == 0);
+        int pend[2] = {n_tiles > 0 ? 0 : -1, n_tiles > 0 ? 0 : -1};
         bool ok = true;
+        __half* vh = sm.v[q][0];
+        __half* vl = sm.v[q][1];
         for (int i = 0; i < n_tiles; ++i) {
-            ok = ok && warp_wait(&bar.vfull, (uint32_t)(i & 1), abort);
-            if (producer && ok) pend = -1;
             const int pos0 = p_begin + i * kTileP;
-            const bool tile_ok = ok && tile_page(a, pt_row, pos0) >= 0;
-            uint32_t w[2][4][3];
-            uint32_t sh[2][4];
-#pragma unroll
-            for (int e = 0; e < 2; ++e)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int pt = kSubP * (q + 4 * e) + 8 * (j >> 1) + (lane & 7);
-                    const int blk = 4 * (j & 1) + (lane >> 3);
-                    if (tile_ok && pos0 + pt < p_end) {
-                        const uint8_t* r = sm.vrec + kRecordBytes * pt;
-                        const uint32_t* wp = reinterpret_cast<const uint32_t*>(r + 12 * blk);
-                        w[e][j][0] = wp[0]; w[e][j][1] = wp[1]; w[e][j][2] = wp[2];
-                        sh[e][j] = *reinterpret_cast<const unsigned short*>(r + 96 + 2 * blk);
-                    } else {
-                        w[e][j][0] = w[e][j][1] = w[e][j][2] = 0u;
-                        sh[e][j] = 0u;
-                    }
-                }
-            named_sync(kBarB2, 128);   // the stage is read: refill it with tile i + 1
-            if (producer && ok && i + 1 < n_tiles && !*abort) {
-                issue_tile_copy(a, pt_row, g, 1, pos0 + kTileP, sm.vrec, &bar.vfull);
-                pend = i + 1;
-            }
-#pragma unroll
+            const bool page_ok = tile_page(a, pt_row, pos0) >= 0;
+#pragma unroll 1
             for (int e = 0; e < 2; ++e) {
-                const int k = 2 * i + e;                 // use of buffer q
+                const int r0 = kSubP * (q + 4 * e);          // first position of the sub-tile
+                ok = ok && warp_wait(&bar.vfull[q][e], (uint32_t)(i & 1), abort);
+                if (producer && ok) pend[e] = -1;
+                const int k = 2 * i + e;                     // use of buffer q
                 if (k >= 1) ok = ok && warp_wait(&bar.v_free[q], (uint32_t)((k - 1) & 1), abort);
-                __half* vh = sm.v[q][0];
-                __half* vl = sm.v[q][1];
-#pragma unroll
+                const uint8_t* rb = sm.vrec + kRecordBytes * r0;
+#pragma unroll 1
                 for (int j = 0; j < 4; ++j) {
                     const int pl = 8 * (j >> 1) + (lane & 7);
                     const int blk = 4 * (j & 1) + (lane >> 3);
+                    uint32_t w3[3];
+                    __half s = __ushort_as_half((unsigned short)0);
+                    if (ok && page_ok && pos0 + r0 + pl < p_end) {
+                        const uint8_t* r = rb + kRecordBytes * pl;
+                        const uint32_t* wp = reinterpret_cast<const uint32_t*>(r + 12 * blk);
+                        w3[0] = wp[0]; w3[1] = wp[1]; w3[2] = wp[2];
+                        s = *reinterpret_cast<const __half*>(r + 96 + 2 * blk);
+                        range_bad |= !(__half2float(s) <= kMaxScale);
+                    } else {
+                        w3[0] = w3[1] = w3[2] = 0u;
+                    }
                     uint32_t hi[16], lo[16];
-                    const __half s = __ushort_as_half((unsigned short)sh[e][j]);
-                    dequant_block(w[e][j], s, hi, lo);
-                    range_bad |= !(__half2float(s) <= kMaxScale);
+                    dequant_block(w3, s, hi, lo);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const int d0 = 32 * blk + 8 * c;
@@ -871,11 +884,20 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                     }
                 }
                 fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.v_ready[q]);
+                __syncwarp();   // this warp's records of the sub-tile are read and its V_hat stored
+                if (producer) {
+                    mbar_arrive(&bar.v_ready[q]);
+                    if (ok && i + 1 < n_tiles && !*abort) {
+                        issue_rec_copy(a, pt_row, g, 1, pos0 + kTileP, r0, kSubP, sm.vrec + kRecordBytes * r0,
+                                       &bar.vfull[q][e]);
+                        pend[e] = i + 1;
+                    }
+                }
             }
         }
-        if (producer && pend >= 0) mbar_drain(&bar.vfull, (uint32_t)(pend & 1));
+        if (producer)
+            for (int e = 0; e < 2; ++e)
+                if (pend[e] >= 0) mbar_drain(&bar.vfull[q][e], (uint32_t)(pend[e] & 1));
     } else if (warp < 14) {
         // ================================================================ MQa / MQb: QK halves
         const int h = warp - 12;                     // 0: dims 0..127 -> S_a, 1: dims 128..255 -> S_b
@@ -890,11 +912,12 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
             if (i >= 1 && !warp_wait(&bar.s_free, (uint32_t)((i - 1) & 1), abort)) break;
             tc_fence_after();
             if (lane == 0) {
-#pragma unroll
+#pragma unroll 1
                 for (int j = 0; j < 8; ++j) {   // descriptor start address is in 16-byte units
-                    mma_ts(dS, aK_hi + 8 * j, bq_hi + (uint64_t)(16 * j), idesc_qk, j > 0 ? 1u : 0u);
-                    mma_ts(dS, aK_hi + 8 * j, bq_lo + (uint64_t)(16 * j), idesc_qk, 1u);
-                    mma_ts(dS, aK_lo + 8 * j, bq_hi + (uint64_t)(16 * j), idesc_qk, 1u);
+                    const uint64_t ko = (uint64_t)(16 * j);
+                    mma_ts(dS, aK_hi + 8 * j, bq_hi + ko, idesc_qk, j > 0 ? 1u : 0u);
+                    mma_ts(dS, aK_hi + 8 * j, bq_lo + ko, idesc_qk, 1u);
+                    mma_ts(dS, aK_lo + 8 * j, bq_hi + ko, idesc_qk, 1u);
                 }
                 mma_commit(&bar.qk_done[h]);
             }
