@@ -170,7 +170,8 @@ Q3KV_API int q3kv_append(void* stream, const q3kv_cache_desc* desc, void* d_pool
  *          (multiple of 256; 0 = chosen from the shape and the GPU)
  *   workspace, workspace_bytes: device scratch of at least
  *          q3kv_workspace_bytes(...) bytes for the same arguments (split
- *          partials; no initial contents needed).  Calls that share one
+ *          partials and, for the tensor-core leg, the rotated queries; no
+ *          initial contents needed).  Calls that share one
  *          workspace must not overlap on the GPU.
  * Slots with T_b == 0 produce nothing.  T_b > L_b or L_b beyond the slot's
  * page table sets Q3KV_STATUS_BAD_LENGTH and the slot's rows are left as they

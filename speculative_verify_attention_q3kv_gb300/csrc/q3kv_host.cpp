@@ -51,7 +51,8 @@ struct Plan {
     int num_splits;
     size_t part_o_bytes;
     size_t part_ml_bytes;
-    size_t total() const { return part_o_bytes + part_ml_bytes; }
+    size_t q_prep_bytes;
+    size_t total() const { return part_o_bytes + part_ml_bytes + q_prep_bytes; }
 };
 
 // Split-K policy: enough (slot, kv head, row chunk, split) CTAs to cover the
@@ -86,6 +87,7 @@ int make_plan(const q3kv_cache_desc* d, int32_t num_slots, int64_t max_ctx, int3
     p->part_o_bytes = (size_t)(units * p->num_splits * p->rows_per_chunk * kHeadDim) * sizeof(float);
     p->part_ml_bytes = (size_t)(units * p->num_splits * p->rows_per_chunk * 2) * sizeof(float);
     if (p->num_splits == 1) p->part_o_bytes = p->part_ml_bytes = 0;
+    p->q_prep_bytes = (impl == Q3KV_IMPL_MMA) ? (size_t)units * kQPrepBytes : 0;
     return Q3KV_OK;
 }
 
@@ -272,6 +274,7 @@ int q3kv_verify_attn(void* stream, const q3kv_cache_desc* desc, const void* d_po
     uint8_t* ws = static_cast<uint8_t*>(d_workspace);
     a.part_o = p.part_o_bytes ? reinterpret_cast<float*>(ws) : nullptr;
     a.part_ml = p.part_ml_bytes ? reinterpret_cast<float*>(ws + p.part_o_bytes) : nullptr;
+    a.q_prep = p.q_prep_bytes ? static_cast<void*>(ws + p.part_o_bytes + p.part_ml_bytes) : nullptr;
     a.status = d_status;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool mma = (p.impl == Q3KV_IMPL_MMA);

@@ -46,6 +46,7 @@ struct VerifyArgs {
     int32_t row_chunks;        // CTAs along the query rows of one kv head
     float* part_o;             // [slots, kv_heads, row_chunks, splits, rows_per_chunk, 256]
     float* part_ml;            // [slots, kv_heads, row_chunks, splits, rows_per_chunk, 2]
+    void* q_prep;              // tensor-core leg: [unit][hi|lo][64 x 256] fp16 rotated queries
     int32_t* status;
 };
 
@@ -72,8 +73,10 @@ struct AppendArgs {
 constexpr int kFmaRows = 64;
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_verify_fma(const VerifyArgs& a, cudaStream_t stream);
-// tcgen05 leg: 64 rows per CTA, one CTA per SM (shared memory bound).
+// tcgen05 leg: 64 rows per CTA, one CTA per SM (shared memory bound); the
+// rotated fp16 hi/lo queries of one unit, as the kernel's B operand of QK.
 constexpr int kMmaRows = 64;
+constexpr size_t kQPrepBytes = 2 * (size_t)kMmaRows * kHeadDim * 2;
 cudaError_t launch_verify_mma(const VerifyArgs& a, cudaStream_t stream);
 // Split-K combine + inverse rotation (after either leg when num_splits > 1).
 cudaError_t launch_merge(const VerifyArgs& a, int rows_per_chunk, bool log2_units, cudaStream_t stream);

@@ -1,11 +1,18 @@
 // Split-K merge for both verify legs (the flash-decode combine step).
 //
-// One CTA per (query row, unit) where unit = (slot, kv head, row chunk); its
-// 256 threads read the partials as float4 over four groups of splits at once.
+// One CTA per (query row, unit) where unit = (slot, kv head, row chunk).
 // For a row with partials (m_i, l_i, o_i) from splits i:
 //   M = max_i m_i,  w_i = e^(m_i - M) / sum_j e^(m_j - M) l_j,  o = sum_i w_i o_i
 // (base-2 exponentials for the tensor-core leg, whose scores are in log2
 // units), then out = H o / 16 back in the unrotated basis.
+//
+// The kernel is launched with programmatic stream serialisation: its CTAs may
+// start while the verify kernel finishes and wait (griddepcontrol.wait) for
+// its results before the first read.  Right after the wait each thread
+// issues the loads of up to 24 partial rows of its split group (256 threads =
+// 4 split groups x 64 float4 columns) together with the (m, l) pairs, which
+// are read once; one warp finishes the row with register/shuffle butterflies
+// for H.
 #include <math_constants.h>
 
 #include "q3kv_common.cuh"
@@ -17,31 +24,34 @@ namespace {
 constexpr int kMergeThreads = 256;
 constexpr int kWChunk = 2048;     // split weights staged in shared memory at a time
 
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float* scratch) {
+__device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float w = __shfl_xor_sync(0xffffffffu, v, o);
-        v = is_max ? fmaxf(v, w) : v + w;
-    }
-    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float r = scratch[0];
-    for (int i = 1; i < kMergeThreads / 32; ++i) r = is_max ? fmaxf(r, scratch[i]) : r + scratch[i];
-    __syncthreads();
-    return r;
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
 }
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <bool LOG2>
+__device__ __forceinline__ float pexp(float x) { return LOG2 ? exp2f(x) : expf(x); }
 
 template <bool LOG2>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(VerifyArgs a, int rows_per_chunk) {
     __shared__ float w[kWChunk];
-    __shared__ float row[kHeadDim];
-    __shared__ float scratch[kMergeThreads / 32];
-    const int tid = threadIdx.x;
+    __shared__ __align__(16) float4 part[4][64];
+    __shared__ float red[2][kMergeThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = blockIdx.x;
     const int unit = blockIdx.y;
     const int chunk = unit % a.row_chunks;
     const int g = (unit / a.row_chunks) % a.num_kv_heads;
     const int slot = unit / (a.row_chunks * a.num_kv_heads);
+
+    // the verify kernel's partials (and the lengths it validated) are complete
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const int T = a.n_q[slot];
     const int L = a.ctx_len[slot];
@@ -53,35 +63,96 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(VerifyArgs a, int 
     const int n_splits = (n_pages + a.split_pages - 1) / a.split_pages;
     if (n_splits <= 1 || n_splits > a.num_splits) return;   // single split: the verify kernel wrote the row
 
-    const float* pml = a.part_ml + ((int64_t)unit * a.num_splits * rows_per_chunk + r) * 2;
-    const int64_t ml_stride = (int64_t)rows_per_chunk * 2;
+    const float2* pml = reinterpret_cast<const float2*>(a.part_ml) + ((int64_t)unit * a.num_splits * rows_per_chunk + r);
+    const int64_t ml_stride = rows_per_chunk;
     const int64_t o_stride = (int64_t)rows_per_chunk * kHeadDim;
 
-    float M = -CUDART_INF_F;
-    for (int i = tid; i < n_splits; i += kMergeThreads) M = fmaxf(M, __ldcg(pml + i * ml_stride));
-    M = block_reduce(M, true, scratch);
-    float den = 0.0f;
-    for (int i = tid; i < n_splits; i += kMergeThreads) {
-        const float mi = __ldcg(pml + i * ml_stride);
-        if (mi != -CUDART_INF_F) den += (LOG2 ? exp2f(mi - M) : expf(mi - M)) * __ldcg(pml + i * ml_stride + 1);
+    // ---- the first kOPre partial rows of each split group are loaded now,
+    // alongside the (m, l) pairs, so both reads overlap in one round trip
+    const int sg = tid >> 6, c = tid & 63;          // split group of 4, float4 column
+    const float* po4 = a.part_o + ((int64_t)unit * a.num_splits * rows_per_chunk + r) * kHeadDim + 4 * c;
+    constexpr int kOPre = 24;
+    float4 ov[kOPre];
+#pragma unroll
+    for (int k = 0; k < kOPre; ++k) {
+        const int i = sg + 4 * k;
+        ov[k] = i < n_splits ? __ldcg(reinterpret_cast<const float4*>(po4 + i * o_stride)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    den = block_reduce(den, false, scratch);
+
+    // ---- M, the denominator and the weights from one read of the (m, l)
+    // pairs (held in registers when there are at most 2048 splits)
+    constexpr int kPerThread = kWChunk / kMergeThreads;
+    const bool in_regs = n_splits <= kWChunk;
+    float2 ml[kPerThread];
+    float M = -CUDART_INF_F;
+    for (int i0 = 0; i0 < n_splits; i0 += kWChunk) {
+#pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+            const int i = i0 + k * kMergeThreads + tid;
+            ml[k] = i < n_splits ? __ldcg(pml + i * ml_stride) : make_float2(-CUDART_INF_F, 0.0f);
+            M = fmaxf(M, ml[k].x);
+        }
+    }
+    M = warp_max(M);
+    if (lane == 0) red[0][warp] = M;
+    __syncthreads();
+    M = red[0][0];
+#pragma unroll
+    for (int k = 1; k < kMergeThreads / 32; ++k) M = fmaxf(M, red[0][k]);
+    float den = 0.0f;
+    if (in_regs) {
+#pragma unroll
+        for (int k = 0; k < kPerThread; ++k)
+            if (ml[k].x != -CUDART_INF_F) {
+                ml[k].x = pexp<LOG2>(ml[k].x - M);   // e^(m_i - M)
+                den += ml[k].x * ml[k].y;
+            } else {
+                ml[k].x = 0.0f;
+            }
+    } else {
+        for (int i = tid; i < n_splits; i += kMergeThreads) {
+            const float2 v = __ldcg(pml + i * ml_stride);
+            if (v.x != -CUDART_INF_F) den += pexp<LOG2>(v.x - M) * v.y;
+        }
+    }
+    den = warp_sum(den);
+    if (lane == 0) red[1][warp] = den;
+    __syncthreads();
+    den = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kMergeThreads / 32; ++k) den += red[1][k];
     const float inv = 1.0f / den;
 
-    // thread = (split group sg of 4, dims 4c..4c+3): float4 loads, four groups
-    // of splits in flight at once, combined through shared memory
-    const int sg = tid >> 6, c = tid & 63;
-    const float* po4 = a.part_o + ((int64_t)unit * a.num_splits * rows_per_chunk + r) * kHeadDim + 4 * c;
+    // ---- o = sum_i w_i o_i
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     for (int i0 = 0; i0 < n_splits; i0 += kWChunk) {
         const int ni = min(kWChunk, n_splits - i0);
-        for (int i = tid; i < ni; i += kMergeThreads) {
-            const float mi = __ldcg(pml + (i0 + i) * ml_stride);
-            w[i] = (mi == -CUDART_INF_F) ? 0.0f : (LOG2 ? exp2f(mi - M) : expf(mi - M)) * inv;
+        if (in_regs) {
+#pragma unroll
+            for (int k = 0; k < kPerThread; ++k) {
+                const int i = k * kMergeThreads + tid;
+                if (i < ni) w[i] = ml[k].x * inv;
+            }
+        } else {
+            for (int i = tid; i < ni; i += kMergeThreads) {
+                const float2 v = __ldcg(pml + (i0 + i) * ml_stride);
+                w[i] = (v.x == -CUDART_INF_F) ? 0.0f : pexp<LOG2>(v.x - M) * inv;
+            }
         }
         __syncthreads();
-#pragma unroll 4
-        for (int i = sg; i < ni; i += 4) {
+        int i = sg;
+        if (i0 == 0) {
+#pragma unroll
+            for (int k = 0; k < kOPre; ++k, i += 4) {
+                const float wi = i < ni ? w[i] : 0.0f;
+                acc.x = fmaf(wi, ov[k].x, acc.x);
+                acc.y = fmaf(wi, ov[k].y, acc.y);
+                acc.z = fmaf(wi, ov[k].z, acc.z);
+                acc.w = fmaf(wi, ov[k].w, acc.w);
+            }
+        }
+#pragma unroll 8
+        for (; i < ni; i += 4) {
             const float4 v = __ldcg(reinterpret_cast<const float4*>(po4 + (i0 + i) * o_stride));
             const float wi = w[i];
             acc.x = fmaf(wi, v.x, acc.x);
@@ -91,34 +162,67 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(VerifyArgs a, int 
         }
         __syncthreads();
     }
-    float4* part = reinterpret_cast<float4*>(w);     // [4 groups][64 quads]
-    part[sg * 64 + c] = acc;
+    part[sg][c] = acc;
     __syncthreads();
-    if (tid < 64) {
-        float4 t = part[tid];
+    if (warp != 0) return;
+
+    // ---- one warp: sum the split groups, out = H o / 16 (lane holds dims 8 lane .. 8 lane + 7)
+    float x[8];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float4 t = part[0][2 * lane + h];
 #pragma unroll
         for (int k = 1; k < 4; ++k) {
-            const float4 u = part[k * 64 + tid];
+            const float4 u = part[k][2 * lane + h];
             t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
         }
-        row[4 * tid] = t.x; row[4 * tid + 1] = t.y; row[4 * tid + 2] = t.z; row[4 * tid + 3] = t.w;
+        x[4 * h] = t.x; x[4 * h + 1] = t.y; x[4 * h + 2] = t.z; x[4 * h + 3] = t.w;
     }
-    __syncthreads();
-    rotate_rows(row, 1);
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if ((i & h) == 0) {
+                const float lo = x[i], hi = x[i + h];
+                x[i] = lo + hi;
+                x[i + h] = lo - hi;
+            }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
+            x[i] = upper ? o - x[i] : x[i] + o;
+        }
+    }
     const int ra = row0 + r;
     const int Hq = a.num_kv_heads * kGroup;
-    a.out[(((int64_t)a.q_offsets[slot] + ra / kGroup) * Hq + g * kGroup + ra % kGroup) * kHeadDim + tid] =
-        row[tid] * 0.0625f;
+    float* dst = a.out + (((int64_t)a.q_offsets[slot] + ra / kGroup) * Hq + g * kGroup + ra % kGroup) * kHeadDim + 8 * lane;
+    reinterpret_cast<float4*>(dst)[0] = make_float4(x[0] * 0.0625f, x[1] * 0.0625f, x[2] * 0.0625f, x[3] * 0.0625f);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(x[4] * 0.0625f, x[5] * 0.0625f, x[6] * 0.0625f, x[7] * 0.0625f);
+}
+
+template <bool LOG2>
+cudaError_t launch(const VerifyArgs& a, int rows_per_chunk, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rows_per_chunk, (unsigned)(a.num_slots * a.num_kv_heads * a.row_chunks));
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_kernel<LOG2>, a, rows_per_chunk);
 }
 
 }  // namespace
 
 cudaError_t launch_merge(const VerifyArgs& a, int rows_per_chunk, bool log2_units, cudaStream_t stream) {
     if (a.num_splits <= 1) return cudaSuccess;
-    dim3 grid((unsigned)rows_per_chunk, (unsigned)(a.num_slots * a.num_kv_heads * a.row_chunks));
-    if (log2_units) merge_kernel<true><<<grid, kMergeThreads, 0, stream>>>(a, rows_per_chunk);
-    else merge_kernel<false><<<grid, kMergeThreads, 0, stream>>>(a, rows_per_chunk);
-    return cudaGetLastError();
+    return log2_units ? launch<true>(a, rows_per_chunk, stream) : launch<false>(a, rows_per_chunk, stream);
 }
 
 }  // namespace q3kv

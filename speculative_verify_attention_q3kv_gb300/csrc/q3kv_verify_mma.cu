@@ -114,6 +114,7 @@ struct Bars {
     unsigned long long kready[2];   // K_hat dims half in TMEM (4 B1 warps)
     unsigned long long qk_done[2];  // S_a / S_b written, that K_hat half read (1 commit)
     unsigned long long s_free;      // S read (4 A warps)
+    unsigned long long q_ready;     // Q hi/lo copied in (bulk copy bytes)
     unsigned long long p_ready[2];  // P^T buffer b stored, O^T rescaled (4 A warps)
     unsigned long long v_ready[4];  // V_hat buffer b filled (its B2 warp)
     unsigned long long v_free[4];   // V_hat buffer b read (2 commits)
@@ -456,10 +457,85 @@ __device__ __forceinline__ __half scale_of(const uint32_t (&sc)[4], int b) {
     return __ushort_as_half((unsigned short)((b & 1) ? (u >> 16) : (u & 0xFFFFu)));
 }
 
+// Rotated queries of one unit (slot, kv head, 64-row chunk) in the verify
+// kernel's shared-memory operand layout, fp16 hi then lo; padding rows are
+// zeros.  One CTA per unit, eight rows per warp (loads first), register
+// butterflies for H, then scale 1/16 (H) * 1/16 (softmax) * log2(e) and a
+// round-to-nearest hi/lo split.
+template <typename TIn>
+__global__ void __launch_bounds__(256) qprep_kernel(VerifyArgs a) {
+    // the verify grid may start now; it waits for this grid before reading Q
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int unit = blockIdx.x;
+    const int chunk = unit % a.row_chunks;
+    const int g = (unit / a.row_chunks) % a.num_kv_heads;
+    const int slot = unit / (a.row_chunks * a.num_kv_heads);
+    const int T = a.n_q[slot];
+    const int row0 = chunk * kRows;
+    const int Rc = max(0, min(kRows, kGroup * min(T, a.max_n_q) - row0));
+    const int Hq = a.num_kv_heads * kGroup;
+    const int64_t q_base = a.q_offsets[slot];
+    __half* qhi = static_cast<__half*>(a.q_prep) + (size_t)unit * (kQPrepBytes / 2);
+    __half* qlo = qhi + kRows * kHeadDim;
+    const TIn* qin = static_cast<const TIn*>(a.q);
+    constexpr int kQRows = kRows / 8;
+    float x[kQRows][8];
+#pragma unroll
+    for (int k = 0; k < kQRows; ++k) {
+        const int r = warp + 8 * k;
+        if (r < Rc) {
+            const int ra = row0 + r;
+            load8(qin + ((q_base + ra / kGroup) * Hq + g * kGroup + ra % kGroup) * kHeadDim + 8 * lane, x[k]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[k][i] = 0.0f;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kQRows; ++k) {
+        const int r = warp + 8 * k;
+        float* y = x[k];
+#pragma unroll
+        for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if ((i & h) == 0) {
+                    const float lo = y[i], hi = y[i + h];
+                    y[i] = lo + hi;
+                    y[i + h] = lo - hi;
+                }
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const float sgn = (lane & m) ? -1.0f : 1.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float o = __shfl_xor_sync(0xffffffffu, y[i], m);
+                y[i] = fmaf(sgn, y[i], o);                // lower lane: o + y, upper lane: o - y
+            }
+        }
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float x0 = y[2 * i] * (1.4426950408889634f / 256.0f);
+            const float x1 = y[2 * i + 1] * (1.4426950408889634f / 256.0f);
+            const __half2 h2 = __floats2half2_rn(x0, x1);
+            const float2 hf = __half22float2(h2);
+            hw[i] = as_u32(h2);
+            lw[i] = as_u32(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
+        }
+        *reinterpret_cast<uint4*>(&qhi[q_off(r, 8 * lane)]) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(&qlo[q_off(r, 8 * lane)]) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+}
+
 template <typename TIn>
 __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     MmaSmem& sm = *reinterpret_cast<MmaSmem*>(smem_raw);
+    // the split-merge kernel may be scheduled once every CTA of this grid runs;
+    // it waits for this grid's completion before reading the partials
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
@@ -498,7 +574,9 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
     volatile int* abort = &sm.abort;
     Bars& bar = sm.bar;
 
-    // ---- set-up: barriers, first record copies, TMEM, row state, queries
+    // ---- set-up: barriers, TMEM, row state; then the first tile's record
+    // copies (K/V warps, which start dequantising at once) and the queries
+    // (softmax and issuer warps, published through q_ready)
     if (tid == 0) {
         for (int q = 0; q < 4; ++q) {
             mbar_init(&bar.kfull[q], 1);
@@ -512,6 +590,7 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
             mbar_init(&bar.pv_done[h], 2);
         }
         mbar_init(&bar.s_free, 4);
+        mbar_init(&bar.q_ready, 1);
         for (int b = 0; b < kVBufs; ++b) {
             mbar_init(&bar.v_ready[b], 1);
             mbar_init(&bar.v_free[b], 2);
@@ -520,10 +599,19 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         sm.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (warp == 12) tmem_alloc(&sm.tmem_base, kTmemCols);
+    if (tid < kRows) {
+        // padding rows (>= Rc) get a running maximum of 0 and a threshold no
+        // score exceeds: they never trigger a rescale and are never stored
+        sm.m_run[tid] = (tid < Rc) ? kMInit : 0.0f;
+        sm.thr[tid] = (tid < Rc) ? kMInit + kRescaleThreshold : CUDART_INF_F;
+        sm.l_run[tid] = 0.0f;
+    }
+    tc_fence_before();
     __syncthreads();
-    // the first tile's records stream in while the queries are prepared:
-    // each dequantising warp copies its own positions
+    tc_fence_after();
     if (warp >= 4 && warp < 12 && lane == 0 && n_tiles > 0) {
+        // each dequantising warp copies its own positions of the first tile
         const int q = warp & 3;
         if (warp < 8) {
             issue_rec_copy(a, pt_row, g, 0, p_begin, 32 * q, 32, sm.krec + kRecordBytes * 32 * q, &bar.kfull[q]);
@@ -534,70 +622,15 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
             }
         }
     }
-    if (warp == 12) tmem_alloc(&sm.tmem_base, kTmemCols);
-    if (tid < kRows) {
-        // padding rows (>= Rc) get a running maximum of 0 and a threshold no
-        // score exceeds: they never trigger a rescale and are never stored
-        sm.m_run[tid] = (tid < Rc) ? kMInit : 0.0f;
-        sm.thr[tid] = (tid < Rc) ? kMInit + kRescaleThreshold : CUDART_INF_F;
-        sm.l_run[tid] = 0.0f;
+    if (warp == 12 && lane == 0) {
+        // the rotated queries of this unit, written by the query kernel that
+        // precedes this grid: wait for it, then one bulk copy of hi and lo
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        const int unit = (slot * a.num_kv_heads + g) * a.row_chunks + chunk;
+        const uint8_t* src = static_cast<const uint8_t*>(a.q_prep) + (size_t)unit * kQPrepBytes;
+        mbar_arrive_expect_tx(&bar.q_ready, (uint32_t)kQPrepBytes);
+        bulk_g2s(sm.qhi, src, (uint32_t)kQPrepBytes, &bar.q_ready);
     }
-    {   // queries: one warp per row (four rows per warp, loads first), register
-        // butterflies for H, then scale 1/16 (H) * 1/16 (softmax) * log2(e) and
-        // split into fp16 hi + lo
-        const TIn* qin = static_cast<const TIn*>(a.q);
-        constexpr int kRowsPerWarp = kRows / kWarps;
-        float x[kRowsPerWarp][8];
-#pragma unroll
-        for (int k = 0; k < kRowsPerWarp; ++k) {
-            const int r = warp + kWarps * k;
-            if (r < Rc) {
-                const int ra = row0 + r;
-                load8(qin + ((q_base + ra / kGroup) * Hq + g * kGroup + ra % kGroup) * kHeadDim + 8 * lane, x[k]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) x[k][i] = 0.0f;
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < kRowsPerWarp; ++k) {
-            const int r = warp + kWarps * k;
-#pragma unroll
-            for (int h = 1; h < 8; h <<= 1)
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if ((i & h) == 0) {
-                        const float lo = x[k][i], hi = x[k][i + h];
-                        x[k][i] = lo + hi;
-                        x[k][i + h] = lo - hi;
-                    }
-#pragma unroll
-            for (int m = 1; m < 32; m <<= 1) {
-                const bool upper = (lane & m) != 0;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float o = __shfl_xor_sync(0xffffffffu, x[k][i], m);
-                    x[k][i] = upper ? o - x[k][i] : x[k][i] + o;
-                }
-            }
-            uint32_t hw[4], lw[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float x0 = x[k][2 * i] * (1.4426950408889634f / 256.0f);
-                const float x1 = x[k][2 * i + 1] * (1.4426950408889634f / 256.0f);
-                const __half2 h2 = __floats2half2_rn(x0, x1);
-                const float2 hf = __half22float2(h2);
-                hw[i] = as_u32(h2);
-                lw[i] = as_u32(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
-            }
-            *reinterpret_cast<uint4*>(&sm.qhi[q_off(r, 8 * lane)]) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(&sm.qlo[q_off(r, 8 * lane)]) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        }
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     bool range_bad = false;
     float* outs = reinterpret_cast<float*>(sm.qhi);      // [64][256] floats once Q is no longer read
@@ -907,7 +940,8 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         const uint32_t dS = tmem + (h ? kColSb : kColSa);
         const uint32_t aK_hi = tmem + kColKHi + 64 * h;
         const uint32_t aK_lo = tmem + kColKLo + 64 * h;
-        for (int i = 0; i < n_tiles; ++i) {
+        bool qok = warp_wait(&bar.q_ready, 0u, abort);
+        for (int i = 0; qok && i < n_tiles; ++i) {
             if (!warp_wait(&bar.kready[h], (uint32_t)(i & 1), abort)) break;
             if (i >= 1 && !warp_wait(&bar.s_free, (uint32_t)((i - 1) & 1), abort)) break;
             tc_fence_after();
@@ -926,6 +960,7 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         if (lane == 0) mma_commit(&bar.drain[h]);
         __syncwarp();
         mbar_drain(&bar.drain[h], 0);
+        if (h == 0 && !qok && lane == 0) mbar_drain(&bar.q_ready, 0);   // the Q copy, after a timeout
     } else {
         // ================================================================ MP0 / MP1: PV halves
         const int h = warp - 14;                     // O^T dims 128h .. 128h + 127
@@ -986,30 +1021,40 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
     }
 }
 
+template <typename TIn>
+cudaError_t launch_typed(const VerifyArgs& a, cudaStream_t stream, bool& attr_set) {
+    const size_t smem = sizeof(MmaSmem);
+    if (!attr_set) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(verify_mma_kernel<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const unsigned units = (unsigned)(a.num_slots * a.num_kv_heads * a.row_chunks);
+    qprep_kernel<TIn><<<units, 256, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // the verify grid may start while the query kernel runs: only its QK
+    // issuer waits (griddepcontrol.wait) for the queries
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.num_splits, (unsigned)(a.num_kv_heads * a.row_chunks), (unsigned)a.num_slots);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, verify_mma_kernel<TIn>, a);
+}
+
 }  // namespace
 
 cudaError_t launch_verify_mma(const VerifyArgs& a, cudaStream_t stream) {
-    const size_t smem = sizeof(MmaSmem);
-    dim3 grid((unsigned)a.num_splits, (unsigned)(a.num_kv_heads * a.row_chunks), (unsigned)a.num_slots);
     static bool attr_set[2] = {false, false};
-    cudaError_t e = cudaSuccess;
-    if (a.dtype == Q3KV_F32) {
-        if (!attr_set[0]) {
-            e = cudaFuncSetAttribute(verify_mma_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-            attr_set[0] = true;
-        }
-        verify_mma_kernel<float><<<grid, kThreads, smem, stream>>>(a);
-    } else {
-        if (!attr_set[1]) {
-            e = cudaFuncSetAttribute(verify_mma_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem);
-            if (e != cudaSuccess) return e;
-            attr_set[1] = true;
-        }
-        verify_mma_kernel<__nv_bfloat16><<<grid, kThreads, smem, stream>>>(a);
-    }
-    return cudaGetLastError();
+    if (a.dtype == Q3KV_F32) return launch_typed<float>(a, stream, attr_set[0]);
+    return launch_typed<__nv_bfloat16>(a, stream, attr_set[1]);
 }
 
 size_t verify_mma_smem_bytes() { return sizeof(MmaSmem); }
