@@ -15,7 +15,8 @@
 // single fp16 operand per side misses by 10-20x on outlier-heavy caches.  So
 // every operand is carried as an exact or near-exact fp16 pair:
 //   K_hat = (c - 3.5) s = (c - 3.5) s_hi + (c - 3.5) s_lo, with s_hi = s rounded
-//           down to 8 significant bits; both products are exact in fp16;
+//           down to 6 significant bits; both products are exact in fp16 and
+//           each is one fused multiply-add from the code;
 //   V_hat likewise; Q = Q_hi + Q_lo and P = P_hi + P_lo (round-to-nearest
 //   splits); each contraction sums the three leading products
 //   (hi.hi + hi.lo + lo.hi) with fp32 accumulation in TMEM.
@@ -94,7 +95,7 @@ constexpr long long kWaitCycles = 2000000000LL;
 // A waiting thread is suspended (not spinning) until the phase completes or
 // this many nanoseconds pass, so idle warps leave the issue slots to the others.
 constexpr uint32_t kSuspendHintNs = 100000;
-constexpr float kMaxScale = 18688.0f;       // 3.5 * s must stay below the fp16 maximum
+constexpr float kMaxScale = 5696.0f;        // 11.5 * s must stay below the fp16 maximum
 
 // TMEM columns (allocation of 512)
 constexpr uint32_t kColKHi = 0;
@@ -326,29 +327,37 @@ constexpr uint32_t kVLbo = 128, kVSbo = 2 * 128;
 constexpr uint32_t kPLbo = 128, kPSbo = 16 * 128;
 
 // ---------------------------------------------------------------- dequantisation
-// fp16 pair (c_even, c_odd) + 512 from two 3-bit fields at bit offsets off and
-// off+16: 0x6000 is 512 with ulp 0.5, so the code goes in at bit 1.
+// fp16 pair (8 + c_even, 8 + c_odd) from two 3-bit fields at bit offsets off
+// and off + 16: 0x4800 is 8 with ulp 1/128, so a code goes in at bit 7.
 __device__ __forceinline__ uint32_t code_pair_word(uint32_t w, int off) {
-    const uint32_t x = (off >= 1) ? (w >> (off - 1)) : (w << 1);
-    return (x & 0x000E000Eu) | 0x60006000u;
+    const uint32_t x = (off >= 7) ? (w >> (off - 7)) : (w << (7 - off));
+    return (x & 0x03800380u) | 0x48004800u;
 }
 __device__ __forceinline__ uint32_t code_pair_last(uint32_t w0, uint32_t w1, uint32_t w2) {
-    // element 30: bit 15 of w0, w1, w2 -> code bits 0,1,2 (into fp16 mantissa bits 1,2,3)
+    // element 30: bit 15 of w0, w1, w2 -> code bits 0,1,2 (into fp16 mantissa bits 7,8,9)
     // element 31: bit 31 of w0, w1, w2
-    const uint32_t x = ((w0 >> 14) & 0x00020002u) | ((w1 >> 13) & 0x00040004u) | ((w2 >> 12) & 0x00080008u);
-    return x | 0x60006000u;
+    const uint32_t x = ((w0 >> 8) & 0x00800080u) | ((w1 >> 7) & 0x01000100u) | ((w2 >> 6) & 0x02000200u);
+    return x | 0x48004800u;
 }
 
 __device__ __forceinline__ __half2 as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 __device__ __forceinline__ uint32_t as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
-// One 32-element block: 16 pairs of (c - 3.5) s_hi and (c - 3.5) s_lo.
+// One 32-element block: 16 pairs of (c - 3.5) s_hi and (c - 3.5) s_lo, where
+// s_hi keeps the top 6 significant bits of s and s_lo = s - s_hi the other 5.
+// With x = 8 + c, (c - 3.5) s_part = x s_part - 11.5 s_part: the constant
+// 11.5 s_part (5 + 6 bits) and the result (3 + 6 or 3 + 5 bits) are exact in
+// fp16, so one fused multiply-add per half gives each product exactly (for
+// s <= 65504 / 11.5 = 5696; larger scales are flagged).
 __device__ __forceinline__ void dequant_block(const uint32_t* w3, __half s, uint32_t (&hi)[16], uint32_t (&lo)[16]) {
-    const __half s_hi = __ushort_as_half((unsigned short)(__half_as_ushort(s) & 0xFFF8u));
+    const __half s_hi = __ushort_as_half((unsigned short)(__half_as_ushort(s) & 0xFFE0u));
     const __half s_lo = __hsub(s, s_hi);
+    const __half m115 = __ushort_as_half((unsigned short)0xC9C0u);   // -11.5
     const __half2 sh2 = __halves2half2(s_hi, s_hi);
     const __half2 sl2 = __halves2half2(s_lo, s_lo);
-    const __half2 off = __float2half2_rn(515.5f);        // 512 + 3.5
+    const __half ch = __hmul(s_hi, m115), cl = __hmul(s_lo, m115);
+    const __half2 ch2 = __halves2half2(ch, ch);
+    const __half2 cl2 = __halves2half2(cl, cl);
     const uint32_t w0 = w3[0], w1 = w3[1], w2 = w3[2];
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
@@ -359,9 +368,8 @@ __device__ __forceinline__ void dequant_block(const uint32_t* w3, __half s, uint
         } else {
             x = code_pair_last(w0, w1, w2);
         }
-        const __half2 c = __hsub2(as_h2(x), off);         // (c_even - 3.5, c_odd - 3.5), exact
-        hi[m] = as_u32(__hmul2(c, sh2));                   // exact: 3 x 8 significant bits
-        lo[m] = as_u32(__hmul2(c, sl2));                   // exact: 3 x 3 significant bits
+        hi[m] = as_u32(__hfma2(as_h2(x), sh2, ch2));     // (c - 3.5) s_hi, exact
+        lo[m] = as_u32(__hfma2(as_h2(x), sl2, cl2));     // (c - 3.5) s_lo, exact
     }
 }
 
@@ -459,74 +467,65 @@ __device__ __forceinline__ __half scale_of(const uint32_t (&sc)[4], int b) {
 
 // Rotated queries of one unit (slot, kv head, 64-row chunk) in the verify
 // kernel's shared-memory operand layout, fp16 hi then lo; padding rows are
-// zeros.  One CTA per unit, eight rows per warp (loads first), register
-// butterflies for H, then scale 1/16 (H) * 1/16 (softmax) * log2(e) and a
-// round-to-nearest hi/lo split.
+// zeros.  CTA (unit, group of 8 rows), one row per warp: register butterflies
+// for H, then scale 1/16 (H) * 1/16 (softmax) * log2(e) and a round-to-nearest
+// hi/lo split.
 template <typename TIn>
 __global__ void __launch_bounds__(256) qprep_kernel(VerifyArgs a) {
     // the verify grid may start now; it waits for this grid before reading Q
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int unit = blockIdx.x;
+    const int r = 8 * blockIdx.y + warp;                 // row within the unit's 64
     const int chunk = unit % a.row_chunks;
     const int g = (unit / a.row_chunks) % a.num_kv_heads;
     const int slot = unit / (a.row_chunks * a.num_kv_heads);
     const int T = a.n_q[slot];
     const int row0 = chunk * kRows;
     const int Rc = max(0, min(kRows, kGroup * min(T, a.max_n_q) - row0));
-    const int Hq = a.num_kv_heads * kGroup;
-    const int64_t q_base = a.q_offsets[slot];
     __half* qhi = static_cast<__half*>(a.q_prep) + (size_t)unit * (kQPrepBytes / 2);
     __half* qlo = qhi + kRows * kHeadDim;
-    const TIn* qin = static_cast<const TIn*>(a.q);
-    constexpr int kQRows = kRows / 8;
-    float x[kQRows][8];
+    float y[8];
+    if (r < Rc) {
+        const int ra = row0 + r;
+        const int Hq = a.num_kv_heads * kGroup;
+        load8(static_cast<const TIn*>(a.q) + (((int64_t)a.q_offsets[slot] + ra / kGroup) * Hq + g * kGroup + ra % kGroup) *
+                                                 kHeadDim + 8 * lane,
+              y);
+    } else {
 #pragma unroll
-    for (int k = 0; k < kQRows; ++k) {
-        const int r = warp + 8 * k;
-        if (r < Rc) {
-            const int ra = row0 + r;
-            load8(qin + ((q_base + ra / kGroup) * Hq + g * kGroup + ra % kGroup) * kHeadDim + 8 * lane, x[k]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) x[k][i] = 0.0f;
-        }
+        for (int i = 0; i < 8; ++i) y[i] = 0.0f;
     }
 #pragma unroll
-    for (int k = 0; k < kQRows; ++k) {
-        const int r = warp + 8 * k;
-        float* y = x[k];
+    for (int h = 1; h < 8; h <<= 1)
 #pragma unroll
-        for (int h = 1; h < 8; h <<= 1)
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if ((i & h) == 0) {
-                    const float lo = y[i], hi = y[i + h];
-                    y[i] = lo + hi;
-                    y[i + h] = lo - hi;
-                }
-#pragma unroll
-        for (int m = 1; m < 32; m <<= 1) {
-            const float sgn = (lane & m) ? -1.0f : 1.0f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float o = __shfl_xor_sync(0xffffffffu, y[i], m);
-                y[i] = fmaf(sgn, y[i], o);                // lower lane: o + y, upper lane: o - y
+        for (int i = 0; i < 8; ++i)
+            if ((i & h) == 0) {
+                const float lo = y[i], hi = y[i + h];
+                y[i] = lo + hi;
+                y[i + h] = lo - hi;
             }
-        }
-        uint32_t hw[4], lw[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float x0 = y[2 * i] * (1.4426950408889634f / 256.0f);
-            const float x1 = y[2 * i + 1] * (1.4426950408889634f / 256.0f);
-            const __half2 h2 = __floats2half2_rn(x0, x1);
-            const float2 hf = __half22float2(h2);
-            hw[i] = as_u32(h2);
-            lw[i] = as_u32(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
+    for (int m = 1; m < 32; m <<= 1) {
+        const float sgn = (lane & m) ? -1.0f : 1.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float o = __shfl_xor_sync(0xffffffffu, y[i], m);
+            y[i] = fmaf(sgn, y[i], o);                    // lower lane: o + y, upper lane: o - y
         }
-        *reinterpret_cast<uint4*>(&qhi[q_off(r, 8 * lane)]) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4*>(&qlo[q_off(r, 8 * lane)]) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float x0 = y[2 * i] * (1.4426950408889634f / 256.0f);
+        const float x1 = y[2 * i + 1] * (1.4426950408889634f / 256.0f);
+        const __half2 h2 = __floats2half2_rn(x0, x1);
+        const float2 hf = __half22float2(h2);
+        hw[i] = as_u32(h2);
+        lw[i] = as_u32(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
+    }
+    *reinterpret_cast<uint4*>(&qhi[q_off(r, 8 * lane)]) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(&qlo[q_off(r, 8 * lane)]) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
 }
 
 template <typename TIn>
@@ -1031,7 +1030,7 @@ cudaError_t launch_typed(const VerifyArgs& a, cudaStream_t stream, bool& attr_se
         attr_set = true;
     }
     const unsigned units = (unsigned)(a.num_slots * a.num_kv_heads * a.row_chunks);
-    qprep_kernel<TIn><<<units, 256, 0, stream>>>(a);
+    qprep_kernel<TIn><<<dim3(units, kRows / 8), 256, 0, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // the verify grid may start while the query kernel runs: only its QK
