@@ -236,21 +236,42 @@ class Step:
     def kv_bytes_per_layer(self):
         return sum(self.Ltot) * self.w.num_kv_heads * 224
 
-    def run(self, verify_events=None, k_new=None, v_new=None, q=None, out=None):
+    def run(self, append=True, verify=True):
+        """One step: for every layer, append the new K/V then verify the new tokens."""
         api = self.api
-        k_new = self.k_new if k_new is None else k_new
-        v_new = self.v_new if v_new is None else v_new
-        q = self.q if q is None else q
-        out = self.out if out is None else out
         for l in range(self.w.num_layers):
-            api.append(self.desc, self.pool, self.page_table, self.slot_len, self.n_new_d, self.row_off,
-                       self.max_new, l, k_new[l], v_new[l], self.status)
-            if verify_events is not None:
-                verify_events[l][0].record()
-            api.verify_attn(self.desc, self.pool, self.page_table, self.ctx_len, self.n_new_d, self.row_off,
-                            self.max_ctx, self.max_new, l, q[l], out[l], self.ws, self.impl, self.split, self.status)
-            if verify_events is not None:
-                verify_events[l][1].record()
+            if append:
+                api.append(self.desc, self.pool, self.page_table, self.slot_len, self.n_new_d, self.row_off,
+                           self.max_new, l, self.k_new[l], self.v_new[l], self.status)
+            if verify:
+                api.verify_attn(self.desc, self.pool, self.page_table, self.ctx_len, self.n_new_d, self.row_off,
+                                self.max_ctx, self.max_new, l, self.q[l], self.out[l], self.ws, self.impl,
+                                self.split, self.status)
+
+    def launches_per_layer(self):
+        """Our kernels per layer: append; for the tensor-core leg the query kernel and the verify
+        kernel (the CUDA-core leg: the verify kernel); the split merge when the context is split,
+        which is when the workspace holds split partials beyond the tensor-core leg's queries."""
+        mma = self.impl != 1
+        units = self.S * self.w.num_kv_heads * ((8 * self.max_new + 63) // 64)
+        query_bytes = units * 2 * 64 * 256 * 2 if mma else 0
+        split = self.ws.numel() > query_bytes
+        return 1 + (2 if mma else 1) + (1 if split else 0)
+
+    def capture(self, **kw):
+        """The step's launches as one CUDA graph (no host launch gaps when replayed)."""
+        torch = self.torch
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.run(**kw)                     # warm the launch path on the capture stream
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.run(**kw)
+        torch.cuda.synchronize()
+        return graph
 
 
 def run_ours(args, rank, world, local, pg):
@@ -270,11 +291,17 @@ def run_ours(args, rank, world, local, pg):
     for _ in range(max(args.warmup, 3)):
         st.run()
     torch.cuda.synchronize()
+    # the step, and its verify calls alone (for the per-launch roofline), as CUDA graphs
+    g_step = st.capture()
+    g_verify = st.capture(append=False)
+    for _ in range(max(args.warmup, 3)):
+        g_step.replay()
+        g_verify.replay()
+    torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    vev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ly)]
-           for _ in range(args.steps)]
+    vev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clocks = ClockSampler(local)
     barrier(pg)
     torch.cuda.synchronize()
@@ -282,13 +309,18 @@ def run_ours(args, rank, world, local, pg):
     for s in range(args.steps):
         flush.zero_()                       # L2 flush between timed steps (outside the events)
         ev[s][0].record(stream)
-        st.run(verify_events=vev[s])
+        g_step.replay()
         ev[s][1].record(stream)
+    for s in range(args.steps):
+        flush.zero_()
+        vev[s][0].record(stream)
+        g_verify.replay()                   # the step's Ly verify calls back to back
+        vev[s][1].record(stream)
     torch.cuda.synchronize()
     clock_info = clocks.stop()
     barrier(pg)
     step_ms = [a.elapsed_time(b_) for a, b_ in ev]
-    verify_ms = [a.elapsed_time(b_) for row in vev for a, b_ in row]
+    verify_ms = [a.elapsed_time(b_) / Ly for a, b_ in vev for _ in range(Ly)]   # per verify call
     total_s = max_over_ranks(pg, sum(step_ms) / 1e3)
     assert int(st.status.item()) == 0, "device status flagged during the benchmark"
 
@@ -299,18 +331,17 @@ def run_ours(args, rank, world, local, pg):
         hv = st.v_new.cpu().pin_memory()
         hq = st.q.cpu().pin_memory()
         ho = torch.empty(st.out.shape, dtype=torch.float32).pin_memory()
-        dk, dv, dq, do = (torch.empty_like(st.k_new), torch.empty_like(st.v_new), torch.empty_like(st.q),
-                          torch.empty_like(st.out))
         e_ms = []
         for s in range(max(args.warmup, 3) + args.steps):
             flush.zero_()
             a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
-            dq.copy_(hq, non_blocking=True)
-            st.run(k_new=dk, v_new=dv, q=dq, out=do)
-            ho.copy_(do, non_blocking=True)
+            # the step's inputs arrive from pinned host memory into the buffers the graph reads
+            st.k_new.copy_(hk, non_blocking=True)
+            st.v_new.copy_(hv, non_blocking=True)
+            st.q.copy_(hq, non_blocking=True)
+            g_step.replay()
+            ho.copy_(st.out, non_blocking=True)
             b_.record(stream)
             torch.cuda.synchronize()
             if s >= max(args.warmup, 3):
@@ -347,18 +378,19 @@ def run_ours(args, rank, world, local, pg):
         "config": {"workload": w.name, "slots": w.num_slots, "layers": Ly, "kv_heads": w.num_kv_heads,
                    "q_heads": w.num_q_heads, "head_dim": w.head_dim, "ctx": st.ctx, "query_tokens": st.n_new,
                    "page_size": 256, "verify_impl": args.verify_impl, "split_positions": args.split,
-                   "l2": "flushed between timed steps (256 MiB write)", "parallelism": f"replicas{world}"},
+                   "l2": "flushed between timed steps (256 MiB write)", "launch": "CUDA graph per step",
+                   "parallelism": f"replicas{world}"},
         "kv_gbs": kv_bytes * Ly * args.steps / (sum(verify_ms) / 1e3) / 1e9,
         "verify_only_tokens_per_s": tokens_per_step * args.steps / (sum(verify_ms) / 1e3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": NCU_TRAFFIC_BYTES.get(w.key) if args.verify_impl == "auto" else None,
-                     "kernel": "q3kv_verify_attn per layer (verify kernel + split-merge kernel)",
+                     "kernel": "q3kv_verify_attn per layer (query + verify + split-merge kernels)",
                      "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": kv_bytes,
                      "mean_launch_us": mean_verify_s * 1e6},
         "clocks": clock_info,
-        "gpu_launches": args.steps * Ly * (3 if st.ws.numel() > 0 else 2),
+        "gpu_launches": args.steps * Ly * st.launches_per_layer(),
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
