@@ -84,7 +84,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kTileP = 128;                 // positions per tile (MMA M of S^T)
 constexpr int kSubP = 16;                   // positions per V sub-tile (one MMA K step)
 constexpr int kSubTiles = kTileP / kSubP;   // 8
-constexpr int kVBufs = 4;                   // V_hat sub-tile ring
+constexpr int kVBufs = 5;                   // V_hat sub-tile ring (5/8 of a tile)
 constexpr uint32_t kRecTile = kTileP * kRecordBytes;   // 14,336 bytes of records per tile
 constexpr int kRows = 64;                   // max query rows per CTA (MMA N <= 64)
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P <= 256
@@ -110,15 +110,14 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kBarA = 1;                    // the 128 softmax threads
 
 struct Bars {
-    unsigned long long kfull[4];    // K records of B1 warp q's 32 positions landed (bulk copy bytes)
     unsigned long long vfull[4][2]; // V records of B2 warp q's sub-tile q + 4e landed
     unsigned long long kready[2];   // K_hat dims half in TMEM (4 B1 warps)
     unsigned long long qk_done[2];  // S_a / S_b written, that K_hat half read (1 commit)
     unsigned long long s_free;      // S read (4 A warps)
     unsigned long long q_ready;     // Q hi/lo copied in (bulk copy bytes)
     unsigned long long p_ready[2];  // P^T buffer b stored, O^T rescaled (4 A warps)
-    unsigned long long v_ready[4];  // V_hat buffer b filled (its B2 warp)
-    unsigned long long v_free[4];   // V_hat buffer b read (2 commits)
+    unsigned long long v_ready[kVBufs];  // V_hat buffer b filled (one B2 warp)
+    unsigned long long v_free[kVBufs];   // V_hat buffer b read (2 commits)
     unsigned long long pv_done[2];  // all PV MMAs of a tile with P^T buffer b done (2 commits)
     unsigned long long drain[4];    // everything an issuer started is done (1 commit)
 };
@@ -129,8 +128,7 @@ struct __align__(16) MmaSmem {
     __half v[kVBufs][2][kSubP * kHeadDim];  // [buffer][hi|lo]: A of PV, MN-major
     __half phi[2][kTileP * kRows];          // B of PV, MN-major, double-buffered by tile
     __half plo[2][kTileP * kRows];
-    uint8_t krec[kRecTile];                 // record stages (bulk copy destinations);
-    uint8_t vrec[kRecTile];                 // their readers copy them to registers first
+    uint8_t vrec[kRecTile];                 // V record stage: one 16-record copy per sub-tile
     float m_run[kRows];
     float thr[kRows];                       // m_run + threshold
     float l_run[kRows];
@@ -166,8 +164,22 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t 
     return ok != 0;
 }
 
-// Bounded wait; on a timeout marks the CTA aborted and returns false.
+__device__ __forceinline__ bool mbar_test_wait(unsigned long long* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait; on a timeout marks the CTA aborted and returns false.  A
+// phase that is already complete is seen by a non-blocking test first.
 __device__ bool mbar_wait(unsigned long long* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_test_wait(bar, parity)) return true;
     if (*abort) return false;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
@@ -197,6 +209,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                      smem_u32(dst)),
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
+}
+
+// One lane of the (converged) warp, chosen by the hardware.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
 }
 
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -578,7 +601,6 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
     // (softmax and issuer warps, published through q_ready)
     if (tid == 0) {
         for (int q = 0; q < 4; ++q) {
-            mbar_init(&bar.kfull[q], 1);
             mbar_init(&bar.vfull[q][0], 1);
             mbar_init(&bar.vfull[q][1], 1);
         }
@@ -609,16 +631,12 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp >= 4 && warp < 12 && lane == 0 && n_tiles > 0) {
-        // each dequantising warp copies its own positions of the first tile
+    if (warp >= 8 && warp < 12 && lane == 0 && n_tiles > 0) {
+        // each V-dequantising warp copies its own positions of the first tile
         const int q = warp & 3;
-        if (warp < 8) {
-            issue_rec_copy(a, pt_row, g, 0, p_begin, 32 * q, 32, sm.krec + kRecordBytes * 32 * q, &bar.kfull[q]);
-        } else {
-            for (int e = 0; e < 2; ++e) {
-                const int r0 = kSubP * (q + 4 * e);
-                issue_rec_copy(a, pt_row, g, 1, p_begin, r0, kSubP, sm.vrec + kRecordBytes * r0, &bar.vfull[q][e]);
-            }
+        for (int e = 0; e < 2; ++e) {
+            const int r0 = kSubP * (q + 4 * e);
+            issue_rec_copy(a, pt_row, g, 1, p_begin, r0, kSubP, sm.vrec + kRecordBytes * r0, &bar.vfull[q][e]);
         }
     }
     if (warp == 12 && lane == 0) {
@@ -812,49 +830,54 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         const int q = warp - 4;
         const int p = 32 * q + lane;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        const bool producer = (lane == 0);           // each B1 warp copies its own 32 records
-        int pend = n_tiles > 0 ? 0 : -1;             // tile whose copy is issued, not yet seen by the producer
+        // thread p's 112-byte record straight from the pool into registers,
+        // a tile ahead (7 x 16-byte read-only loads)
+        auto fetch = [&](int i, uint32_t (&w)[24], uint32_t (&sc)[4]) {
+            const int pos0 = p_begin + i * kTileP;
+            const int32_t page = (i < n_tiles) ? tile_page(a, pt_row, pos0) : -1;
+            if (page >= 0 && pos0 + p < p_end) {
+                const uint4* r4 = reinterpret_cast<const uint4*>(
+                    a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, 0, pos0 % kPageSize + p));
+#pragma unroll
+                for (int m = 0; m < 6; ++m) {
+                    const uint4 u = __ldg(r4 + m);
+                    w[4 * m] = u.x; w[4 * m + 1] = u.y; w[4 * m + 2] = u.z; w[4 * m + 3] = u.w;
+                }
+                const uint4 u = __ldg(r4 + 6);
+                sc[0] = u.x; sc[1] = u.y; sc[2] = u.z; sc[3] = u.w;
+            } else {
+#pragma unroll
+                for (int m = 0; m < 24; ++m) w[m] = 0u;
+                sc[0] = sc[1] = sc[2] = sc[3] = 0u;
+            }
+        };
+        uint32_t wn[24], sn[4];
+        fetch(0, wn, sn);
         bool ok = true;
         for (int i = 0; i < n_tiles; ++i) {
-            ok = ok && warp_wait(&bar.kfull[q], (uint32_t)(i & 1), abort);
-            if (producer && ok) pend = -1;
-            const int pos0 = p_begin + i * kTileP;
-            const bool valid = ok && tile_page(a, pt_row, pos0) >= 0 && pos0 + p < p_end;
-            const uint8_t* rec = sm.krec + kRecordBytes * p;
+            uint32_t w[24], sc[4];
+#pragma unroll
+            for (int m = 0; m < 24; ++m) w[m] = wn[m];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) sc[m] = sn[m];
+            fetch(i + 1, wn, sn);                    // the next tile's record is in flight meanwhile
+            const bool valid = ok && p_begin + i * kTileP + p < p_end;
             // two halves of the dims, each after its QK half of the previous tile
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
-                uint32_t w[12], sc[2];
-                if (valid) {
-                    const uint4* r4 = reinterpret_cast<const uint4*>(rec + 48 * hh);
+                uint32_t wh[12], sh[2];
 #pragma unroll
-                    for (int m = 0; m < 3; ++m) {
-                        const uint4 u = r4[m];
-                        w[4 * m] = u.x; w[4 * m + 1] = u.y; w[4 * m + 2] = u.z; w[4 * m + 3] = u.w;
-                    }
-                    const uint2 s2 = *reinterpret_cast<const uint2*>(rec + 96 + 8 * hh);
-                    sc[0] = s2.x; sc[1] = s2.y;
-                } else {
-#pragma unroll
-                    for (int m = 0; m < 12; ++m) w[m] = 0u;
-                    sc[0] = sc[1] = 0u;
-                }
-                if (hh == 1) {
-                    __syncwarp();   // this warp's records are read: refill them with tile i + 1
-                    if (producer && ok && i + 1 < n_tiles && !*abort) {
-                        issue_rec_copy(a, pt_row, g, 0, pos0 + kTileP, 32 * q, 32, sm.krec + kRecordBytes * 32 * q,
-                                       &bar.kfull[q]);
-                        pend = i + 1;
-                    }
-                }
+                for (int m = 0; m < 12; ++m) wh[m] = hh ? w[12 + m] : w[m];
+                sh[0] = hh ? sc[2] : sc[0];
+                sh[1] = hh ? sc[3] : sc[1];
                 if (i > 0) ok = ok && warp_wait(&bar.qk_done[hh], (uint32_t)((i - 1) & 1), abort);
                 tc_fence_after();
                 const uint32_t col = tmem + lane_base + 64 * hh;
 #pragma unroll
                 for (int bb = 0; bb < 4; ++bb) {
                     uint32_t hi[16], lo[16];
-                    const __half s = __ushort_as_half((unsigned short)((bb & 1) ? (sc[bb >> 1] >> 16) : (sc[bb >> 1] & 0xFFFFu)));
-                    dequant_block(&w[3 * bb], s, hi, lo);
+                    const __half s = __ushort_as_half((unsigned short)((bb & 1) ? (sh[bb >> 1] >> 16) : (sh[bb >> 1] & 0xFFFFu)));
+                    dequant_block(&wh[3 * bb], s, hi, lo);
                     range_bad |= valid && !(__half2float(s) <= kMaxScale);
                     tmem_st16(col + kColKHi + 16 * bb, hi);
                     tmem_st16(col + kColKLo + 16 * bb, lo);
@@ -865,19 +888,15 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                 if (lane == 0) mbar_arrive(&bar.kready[hh]);
             }
         }
-        // after a timeout: wait (bounded) for a copy still landing in shared memory
-        if (producer && pend >= 0) mbar_drain(&bar.kfull[q], (uint32_t)(pend & 1));
     } else if (warp < 12) {
         // ================================================================ B2: V_hat sub-tiles -> shared memory
-        // Warp q fills ring buffer q with sub-tiles q and q + 4 of every tile,
-        // from its own two 16-record copies.  Lane = (position pl, 32-dim block
+        // Warp q fills sub-tiles q and q + 4 of every tile (sub-tile u = 8 i + s
+        // goes to ring buffer u % 5) from its own two 16-record copies.  Lane = (position pl, 32-dim block
         // blk); item j covers pl = 8 (j >> 1) + (lane & 7), blk = 4 (j & 1) + (lane >> 3).
         const int q = warp - 8;
         const bool producer = (lane == 0);
         int pend[2] = {n_tiles > 0 ? 0 : -1, n_tiles > 0 ? 0 : -1};
         bool ok = true;
-        __half* vh = sm.v[q][0];
-        __half* vl = sm.v[q][1];
         for (int i = 0; i < n_tiles; ++i) {
             const int pos0 = p_begin + i * kTileP;
             const bool page_ok = tile_page(a, pt_row, pos0) >= 0;
@@ -886,8 +905,12 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                 const int r0 = kSubP * (q + 4 * e);          // first position of the sub-tile
                 ok = ok && warp_wait(&bar.vfull[q][e], (uint32_t)(i & 1), abort);
                 if (producer && ok) pend[e] = -1;
-                const int k = 2 * i + e;                     // use of buffer q
-                if (k >= 1) ok = ok && warp_wait(&bar.v_free[q], (uint32_t)((k - 1) & 1), abort);
+                const int u = kSubTiles * i + q + 4 * e;     // sub-tile index: ring buffer u % 5, its use u / 5
+                const int b = u % kVBufs;
+                const int k = u / kVBufs;
+                if (k >= 1) ok = ok && warp_wait(&bar.v_free[b], (uint32_t)((k - 1) & 1), abort);
+                __half* vh = sm.v[b][0];
+                __half* vl = sm.v[b][1];
                 const uint8_t* rb = sm.vrec + kRecordBytes * r0;
 #pragma unroll 1
                 for (int j = 0; j < 4; ++j) {
@@ -918,7 +941,7 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                 fence_proxy_async();
                 __syncwarp();   // this warp's records of the sub-tile are read and its V_hat stored
                 if (producer) {
-                    mbar_arrive(&bar.v_ready[q]);
+                    mbar_arrive(&bar.v_ready[b]);
                     if (ok && i + 1 < n_tiles && !*abort) {
                         issue_rec_copy(a, pt_row, g, 1, pos0 + kTileP, r0, kSubP, sm.vrec + kRecordBytes * r0,
                                        &bar.vfull[q][e]);
@@ -944,16 +967,19 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
             if (!warp_wait(&bar.kready[h], (uint32_t)(i & 1), abort)) break;
             if (i >= 1 && !warp_wait(&bar.s_free, (uint32_t)((i - 1) & 1), abort)) break;
             tc_fence_after();
-            if (lane == 0) {
-#pragma unroll 1
-                for (int j = 0; j < 8; ++j) {   // descriptor start address is in 16-byte units
-                    const uint64_t ko = (uint64_t)(16 * j);
+            // descriptors are formed by the whole (converged) warp, so they stay
+            // warp-uniform; one elected lane issues
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {   // descriptor start address is in 16-byte units
+                const uint64_t ko = (uint64_t)(16 * j);
+                if (elect_one()) {
                     mma_ts(dS, aK_hi + 8 * j, bq_hi + ko, idesc_qk, j > 0 ? 1u : 0u);
                     mma_ts(dS, aK_hi + 8 * j, bq_lo + ko, idesc_qk, 1u);
                     mma_ts(dS, aK_lo + 8 * j, bq_hi + ko, idesc_qk, 1u);
                 }
-                mma_commit(&bar.qk_done[h]);
+                __syncwarp();
             }
+            if (elect_one()) mma_commit(&bar.qk_done[h]);
             __syncwarp();
         }
         if (lane == 0) mma_commit(&bar.drain[h]);
@@ -977,24 +1003,27 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
             bool ok = true;
 #pragma unroll 1
             for (int sub = 0; sub < kSubTiles; ++sub) {
-                // sub-tile sub sits in buffer sub % 4, that buffer's use 2 jt + sub / 4
-                const int b = sub & (kVBufs - 1);
-                ok = warp_wait(&bar.v_ready[b], (uint32_t)((2 * jt + sub / kVBufs) & 1), abort);
+                // sub-tile u = 8 jt + sub sits in buffer u % 5, that buffer's use u / 5
+                const int u = kSubTiles * jt + sub;
+                const int b = u % kVBufs;
+                ok = warp_wait(&bar.v_ready[b], (uint32_t)((u / kVBufs) & 1), abort);
                 if (!ok) break;
                 tc_fence_after();
-                if (lane == 0) {
-                    const uint64_t bfo = (uint64_t)b * vbuf;
-                    const uint64_t koff = (uint64_t)pb * pbuf + (uint64_t)(16 * sub);   // 2 sub x 128 bytes along K
-                    const uint32_t acc0 = (jt > 0 || sub > 0) ? 1u : 0u;
-                    mma_ss(dO, av_hi0 + bfo, bp_hi0 + koff, idesc_pv, acc0);
-                    mma_ss(dO, av_lo0 + bfo, bp_hi0 + koff, idesc_pv, 1u);
-                    mma_ss(dO, av_hi0 + bfo, bp_lo0 + koff, idesc_pv, 1u);
+                // descriptors formed by the whole warp (warp-uniform); one elected lane issues
+                const uint64_t bfo = (uint64_t)b * vbuf;
+                const uint64_t koff = (uint64_t)pb * pbuf + (uint64_t)(16 * sub);   // 2 sub x 128 bytes along K
+                const uint32_t acc0 = (jt > 0 || sub > 0) ? 1u : 0u;
+                const uint64_t avh = av_hi0 + bfo, avl = av_lo0 + bfo, bph = bp_hi0 + koff, bpl = bp_lo0 + koff;
+                if (elect_one()) {
+                    mma_ss(dO, avh, bph, idesc_pv, acc0);
+                    mma_ss(dO, avl, bph, idesc_pv, 1u);
+                    mma_ss(dO, avh, bpl, idesc_pv, 1u);
                     mma_commit(&bar.v_free[b]);
                 }
                 __syncwarp();
             }
             if (!ok) break;
-            if (lane == 0) mma_commit(&bar.pv_done[pb]);
+            if (elect_one()) mma_commit(&bar.pv_done[pb]);
             __syncwarp();
         }
         if (lane == 0) mma_commit(&bar.drain[2 + h]);
