@@ -7,7 +7,9 @@ A plain, slow, obviously correct restatement of what the hot path computes:
 * ``packing``   -- the byte layout of a coded vector and of a cache page;
 * ``attention`` -- multi-token causal verify attention in float64 over the
                    exactly dequantised values, GQA group by group;
-* ``cache``     -- an oracle-side paged cache: append and read back.
+* ``cache``     -- an oracle-side paged cache: append and read back;
+* ``accept``    -- greedy acceptance of a verify step's drafts and the commit
+                   (rollback) of the cache length.
 
 Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
 may import this package.  The product path (the CUDA library and its Python
