@@ -215,6 +215,43 @@ Q3KV_API int q3kv_verify_attn_noalloc(void* stream, const q3kv_cache_desc* desc,
                      const void* q, int32_t dtype, float* out,
                      int32_t impl, int32_t split_positions, int32_t* d_status);
 
+/* ---- greedy acceptance and commit ------------------------------------------
+ * Source: "Quasar" (q27) wiki -- the sampler paragraph of "Serving" and the
+ * "Model tool protocol" bullet (greedy speculative decode is the default), and
+ * the prefix-cache discussion (attention rows below the point where the drafts
+ * diverge are append-only and stay valid in place: a rejected draft is undone
+ * by shortening the length, and the next append overwrites its rows).
+ *
+ * Slot b's verify step had T_b = d_n_q[b] query tokens: t_0 (the last committed
+ * token) then drafts d_1 .. d_{T_b - 1}, at rows d_q_offsets[b] + j of logits
+ * and d_tokens (the same row indexing as q3kv_verify_attn); logits row j
+ * predicts the token after query token j.  With g_j the argmax of row j (the
+ * lowest vocabulary index among equal maxima):
+ *   a    = number of leading drafts with d_{j+1} == g_j      (0 <= a <= T_b - 1)
+ *   next = g_a                     (the correction, or the bonus token if a = T_b - 1)
+ *   committed = ctx_len - (T_b - 1 - a)   (keeps t_0 and the accepted drafts)
+ * Outputs per slot: d_n_accepted[b] = a, d_next_token[b] = next,
+ * d_committed_len[b] = committed.  A slot with T_b == 0 gets (0, -1, ctx_len).
+ *   logits   device [num_rows, vocab], f32 or bf16 (dtype); num_rows bounds
+ *            the rows of all slots (sizes the launch; rows past the slots'
+ *            rows are read but unused)
+ *   d_ctx_len   cache length of each slot after the step's append; may be the
+ *            same array as d_committed_len (in-place commit)
+ *   workspace   device scratch of at least q3kv_accept_workspace_bytes(num_rows,
+ *            vocab) bytes, 8-byte aligned, no initial contents needed; calls
+ *            sharing it must not overlap on the GPU
+ * Errors: Q3KV_ERR_INVALID_ARG / _UNSUPPORTED (num_rows > 65535, max_n_q > 16)
+ * / _WORKSPACE_TOO_SMALL before any launch.  On the device, T_b > max_n_q,
+ * T_b > ctx_len or rows past num_rows set Q3KV_STATUS_BAD_LENGTH and give the
+ * slot (0, -1, ctx_len); a NaN logit sets Q3KV_STATUS_NONFINITE_INPUT (its
+ * row's argmax is then unspecified).  Asynchronous on the stream. */
+Q3KV_API int q3kv_accept_workspace_bytes(int32_t num_rows, int32_t vocab, size_t* bytes);
+Q3KV_API int q3kv_accept_greedy(void* stream, const void* logits, int32_t dtype, int32_t vocab,
+                       const int32_t* d_q_offsets, const int32_t* d_n_q, const int32_t* d_tokens,
+                       int32_t num_slots, int32_t num_rows, int32_t max_n_q, const int32_t* d_ctx_len,
+                       int32_t* d_n_accepted, int32_t* d_next_token, int32_t* d_committed_len,
+                       void* d_workspace, size_t workspace_bytes, int32_t* d_status);
+
 #ifdef __cplusplus
 }
 #endif

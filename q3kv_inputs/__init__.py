@@ -34,6 +34,12 @@ _TAG_KV = 2
 _TAG_KV_CHANNEL = 3
 _TAG_Q = 4
 _TAG_Q_CHANNEL = 5
+_TAG_LOGITS = 6
+_TAG_TOKENS = 7
+
+# Vocabulary size of the acceptance inputs: the padded vocabulary the pages
+# quote for their model family (a synthetic stand-in; no weights are used).
+VOCAB = 248_320
 
 
 @dataclasses.dataclass(frozen=True)
@@ -179,6 +185,26 @@ def q_rows(w: Workload, slot: int, layer: int, step: int, n_q: int) -> np.ndarra
     if w.dtype == "bf16":
         x = round_to_bf16(x)
     return x
+
+
+def logits_rows(seed: int, rows: int, vocab: int, kind: str = "normal", bf16: bool = False) -> np.ndarray:
+    """Synthetic logits float32 [rows, vocab] for the acceptance step.
+
+    kind "normal": N(0, 4) values (distinct maxima); "ties": small integers in
+    [-3, 3] (many equal maxima).  bf16=True rounds them once to bfloat16; that
+    exact array is what both sides are given.
+    """
+    rng = _rng(seed, _TAG_LOGITS, rows, vocab)
+    if kind == "ties":
+        x = rng.integers(-3, 4, size=(rows, vocab)).astype(np.float32)
+    else:
+        x = (2.0 * rng.standard_normal((rows, vocab), dtype=np.float32)).astype(np.float32)
+    return round_to_bf16(x) if bf16 else x
+
+
+def random_tokens(seed: int, rows: int, vocab: int) -> np.ndarray:
+    """Uniform random token ids int32 [rows] (query tokens that are not planted)."""
+    return _rng(seed, _TAG_TOKENS, rows, vocab).integers(0, vocab, size=rows).astype(np.int32)
 
 
 def random_page_table(num_slots: int, pages_per_slot: List[int], num_pages: int, seed: int) -> np.ndarray:

@@ -144,3 +144,23 @@ def verify_attn_noalloc(desc: CacheDesc, pool: torch.Tensor, page_table: torch.T
                                               ctx_len.shape[0], max_ctx_len, max_n_q, layer, _ptr(q),
                                               _dtype_code(q), _ptr(out), impl, split_positions, _ptr(status))
     check(rc, "q3kv_verify_attn_noalloc")
+
+
+def accept_workspace_bytes(num_rows: int, vocab: int) -> int:
+    n = ctypes.c_size_t()
+    check(_lib.load().q3kv_accept_workspace_bytes(num_rows, vocab, ctypes.byref(n)), "q3kv_accept_workspace_bytes")
+    return n.value
+
+
+def accept_greedy(logits: torch.Tensor, q_offsets: torch.Tensor, n_q: torch.Tensor, tokens: torch.Tensor,
+                  max_n_q: int, ctx_len: torch.Tensor, n_accepted: torch.Tensor, next_token: torch.Tensor,
+                  committed_len: torch.Tensor, workspace: Optional[torch.Tensor],
+                  status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """q3kv_accept_greedy: logits [rows, vocab] (f32 or bf16); int32 per-slot outputs."""
+    rows, vocab = logits.shape
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = _lib.load().q3kv_accept_greedy(_stream(stream), _ptr(logits), _dtype_code(logits), vocab, _ptr(q_offsets),
+                                        _ptr(n_q), _ptr(tokens), n_q.shape[0], rows, max_n_q, _ptr(ctx_len),
+                                        _ptr(n_accepted), _ptr(next_token), _ptr(committed_len), _ptr(workspace),
+                                        nbytes, _ptr(status))
+    check(rc, "q3kv_accept_greedy")

@@ -69,6 +69,29 @@ struct AppendArgs {
     int32_t* status;
 };
 
+// Greedy acceptance of a verify step (argmax kernel + acceptance kernel).
+struct AcceptArgs {
+    const void* logits;        // [num_rows, vocab] f32 or bf16
+    int32_t dtype;
+    int32_t vocab;
+    int64_t chunk_elems;       // vocabulary entries per argmax CTA (a multiple of 8)
+    int32_t num_chunks;
+    int32_t vec_ok;            // rows are 16-byte aligned: 16-byte loads
+    const int32_t* q_offsets;
+    const int32_t* n_q;
+    const int32_t* tokens;     // [num_rows] query tokens (t_0, drafts)
+    int32_t num_slots;
+    int32_t num_rows;
+    int32_t max_n_q;
+    const int32_t* ctx_len;
+    int32_t* n_accepted;
+    int32_t* next_token;
+    int32_t* committed_len;
+    void* partial;             // [num_rows, num_chunks] (max, index) pairs
+    int32_t* status;
+};
+cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t stream);
+
 // FMA (CUDA-core) leg: rows per CTA, and its workspace/launch.
 constexpr int kFmaRows = 64;
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);

@@ -131,3 +131,21 @@ def test_argument_checks_launch_nothing(lib):
     args[15] = 1
     args[2] = args[3] = args[5] = args[6] = args[7] = args[12] = args[14] = fake
     assert lib.q3kv_verify_attn(*args) == _lib.Q3KV_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_accept_argument_checks():
+    from speculative_verify_attention_q3kv_gb300 import _lib
+    lib = _lib.load()
+    n = ctypes.c_size_t()
+    assert lib.q3kv_accept_workspace_bytes(-1, 100, ctypes.byref(n)) == _lib.Q3KV_ERR_INVALID_ARG
+    assert lib.q3kv_accept_workspace_bytes(4, 0, ctypes.byref(n)) == _lib.Q3KV_ERR_INVALID_ARG
+    assert lib.q3kv_accept_workspace_bytes(4, 100, None) == _lib.Q3KV_ERR_INVALID_ARG
+    args = [None, 16, _lib.Q3KV_BF16, 100, 16, 16, 16, 1, 4, 4, 16, 16, 16, 16, 16, 64, None]
+    bad_dtype = list(args); bad_dtype[2] = 7
+    assert lib.q3kv_accept_greedy(*bad_dtype) == _lib.Q3KV_ERR_INVALID_ARG
+    bad_vocab = list(args); bad_vocab[3] = 0
+    assert lib.q3kv_accept_greedy(*bad_vocab) == _lib.Q3KV_ERR_INVALID_ARG
+    wide = list(args); wide[9] = 17
+    assert lib.q3kv_accept_greedy(*wide) == _lib.Q3KV_ERR_UNSUPPORTED
+    many_rows = list(args); many_rows[8] = 70000
+    assert lib.q3kv_accept_greedy(*many_rows) == _lib.Q3KV_ERR_UNSUPPORTED

@@ -1,0 +1,130 @@
+"""GPU parity of greedy acceptance and commit (q3kv_accept_greedy) against
+oracle/accept.py: accepted counts, next tokens and committed lengths are
+integers and must match exactly.  Inputs: seeded synthetic logits from
+q3kv_inputs (float32 or bf16-rounded; the oracle gets the exact values the
+kernel reads), drafts planted along the oracle's argmax chain for a chosen
+number of steps, then a wrong token.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import q3kv_inputs as qi
+from gpu_harness import GpuCache, check_close, oracle_verify, slot_kv
+from oracle.accept import greedy_accept
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _plant(logits, offs, nq, keep, seed, vocab):
+    """Query tokens: t_0 random, then `keep[b]` drafts equal to the argmax chain, then wrong ones."""
+    toks = qi.random_tokens(seed, logits.shape[0], vocab)
+    g = logits.argmax(axis=1)
+    for b, T in enumerate(nq):
+        r0 = offs[b]
+        for j in range(1, T):
+            toks[r0 + j] = g[r0 + j - 1] if j <= keep[b] else (g[r0 + j - 1] + 1 + j) % vocab
+    return toks
+
+
+def _run(logits_np, offs, nq, toks, ctx, bf16, max_nq=None, inplace=False):
+    from speculative_verify_attention_q3kv_gb300 import api
+    rows, vocab = logits_np.shape
+    lg = torch.from_numpy(logits_np).cuda()
+    if bf16:
+        lg = lg.to(torch.bfloat16)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    S = len(nq)
+    ctx_d = torch.tensor(np.asarray(ctx, np.int32), **i32)
+    n_acc = torch.full((S,), -7, **i32)
+    nxt = torch.full((S,), -7, **i32)
+    com = ctx_d if inplace else torch.full((S,), -7, **i32)
+    ws = torch.empty(max(api.accept_workspace_bytes(rows, vocab), 8), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, **i32)
+    api.accept_greedy(lg, torch.tensor(np.asarray(offs, np.int32), **i32), torch.tensor(np.asarray(nq, np.int32), **i32),
+                      torch.tensor(np.asarray(toks, np.int32), **i32), max(nq) if max_nq is None else max_nq,
+                      ctx_d, n_acc, nxt, com, ws, st)
+    torch.cuda.synchronize()
+    return n_acc.cpu().numpy(), nxt.cpu().numpy(), com.cpu().numpy(), int(st.item())
+
+
+@pytest.mark.parametrize("vocab", [1000, 4099, 50_257, qi.VOCAB])
+@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("kind", ["normal", "ties"])
+def test_accept_matches_oracle(vocab, bf16, kind):
+    rng = np.random.default_rng(vocab + 7 * bf16)
+    nq = [int(x) for x in rng.integers(0, 17, size=7)]
+    nq[2] = 0                                           # an empty slot
+    nq[0] = 16                                          # the widest verify
+    offs = np.concatenate([[0], np.cumsum(nq)[:-1]]).astype(np.int32)
+    rows = int(sum(nq))
+    logits = qi.logits_rows(vocab, rows, vocab, kind, bf16)
+    keep = [int(rng.integers(0, max(T, 1))) for T in nq]
+    keep[0] = 15                                        # every draft of slot 0 accepted
+    toks = _plant(logits, offs, nq, keep, vocab, vocab)
+    ctx = [int(x) for x in rng.integers(20, 5000, size=7)]
+    want = greedy_accept(logits.astype(np.float64), offs, nq, toks, ctx)
+    got = _run(logits, offs, nq, toks, ctx, bf16)
+    assert got[3] == 0
+    for w_, g_ in zip(want, got[:3]):
+        assert np.array_equal(w_, g_), (w_, g_)
+
+
+def test_accept_in_place_commit_and_status():
+    vocab = 3000
+    nq = [6, 3]
+    offs = [0, 6]
+    logits = qi.logits_rows(1, 9, vocab)
+    toks = _plant(logits, offs, nq, [2, 1], 1, vocab)
+    ctx = [40, 9]
+    want = greedy_accept(logits.astype(np.float64), offs, nq, toks, ctx)
+    n_acc, nxt, com, st = _run(logits, offs, nq, toks, ctx, False, inplace=True)
+    assert st == 0
+    assert np.array_equal(n_acc, want[0]) and np.array_equal(nxt, want[1]) and np.array_equal(com, want[2])
+    # more query tokens than the launch bound: BAD_LENGTH, the slot keeps its length
+    n_acc, nxt, com, st = _run(logits, offs, nq, toks, ctx, False, max_nq=4)
+    assert st & 8
+    assert (n_acc[0], nxt[0], com[0]) == (0, -1, 40)
+    assert (n_acc[1], nxt[1], com[1]) == (want[0][1], want[1][1], want[2][1])
+    # a NaN logit is flagged
+    bad = logits.copy()
+    bad[7, 11] = np.nan
+    st = _run(bad, offs, nq, toks, ctx, False)[3]
+    assert st & 1
+
+
+def test_step_accept_commit_then_next_step_overwrites_rejected_rows():
+    """Verify step 1 (t_0 + 5 drafts), accept 2 drafts, commit; step 2 appends its
+    tokens at the committed length over the rejected rows and verifies: the
+    result equals the oracle over the accepted sequence only."""
+    w = dataclasses.replace(qi.WORKLOADS[1], num_slots=1, name="accept-e2e")
+    c = GpuCache(w, [400], num_layers=1)
+    n0, T = 300, 6
+    k, v = slot_kv(w, 0, 0, 0, n0 + T)
+    c.append_rows(0, [0], [0], [(k, v)])                          # context + t_0 + 5 drafts
+    q1 = qi.q_rows(w, 0, 0, 0, T)
+    check_close(c.verify(0, [n0 + T], [T], [q1], impl=2), oracle_verify(w, 0, 0, n0, q1, k, v))
+    vocab = 5000
+    logits = qi.logits_rows(3, T, vocab)
+    toks = _plant(logits, [0], [T], [2], 3, vocab)
+    n_acc, nxt, com, st = _run(logits, [0], [T], toks, [n0 + T], False)
+    assert st == 0 and n_acc[0] == 2 and com[0] == n0 + 3
+    # step 2: next token + 4 new drafts appended at the committed length
+    rng = np.random.default_rng(5)
+    T2 = 5
+    k2 = rng.standard_normal((T2, 2, 256)).astype(np.float32)
+    v2 = rng.standard_normal((T2, 2, 256)).astype(np.float32)
+    c.append_rows(0, [0], [int(com[0])], [(k2, v2)])
+    kk = np.concatenate([k[: int(com[0])], k2])
+    vv = np.concatenate([v[: int(com[0])], v2])
+    q2 = qi.q_rows(w, 0, 0, 1, T2)
+    out = c.verify(0, [int(com[0]) + T2], [T2], [q2], impl=2)
+    check_close(out, oracle_verify(w, 0, 0, int(com[0]), q2, kk, vv))
