@@ -208,6 +208,16 @@ class Step:
                 qi.torch_fill_kv_(self.k_new[l, :, h], w, l, h, 0, g)
                 qi.torch_fill_kv_(self.v_new[l, :, h], w, l, h, 1, g)
         self.out = torch.empty((Ly, self.rows, Hq, D), dtype=torch.float32, device=device)
+        # acceptance after the step: synthetic logits of the step's query tokens, a
+        # Qwen-class vocabulary; outputs kept apart so the lengths stay fixed between steps
+        self.vocab = qi.VOCAB
+        self.logits = torch.randn((self.rows, self.vocab), generator=g, device=device).to(torch.bfloat16)
+        self.tokens = torch.from_numpy(qi.random_tokens(w.seed, self.rows, self.vocab)).to(device)
+        self.n_acc = torch.zeros(self.S, **i32)
+        self.next_tok = torch.zeros(self.S, **i32)
+        self.committed = torch.zeros(self.S, **i32)
+        self.accept_ws = torch.empty(max(api.accept_workspace_bytes(self.rows, self.vocab), 8), dtype=torch.uint8,
+                                     device=device)
         self._prefill(g)
 
     def _prefill(self, g):
@@ -248,6 +258,11 @@ class Step:
                                 self.max_ctx, self.max_new, l, self.q[l], self.out[l], self.ws, self.impl,
                                 self.split, self.status)
 
+    def accept(self):
+        """Greedy acceptance of the step's drafts and the committed lengths (once per step)."""
+        self.api.accept_greedy(self.logits, self.row_off, self.n_new_d, self.tokens, self.max_new, self.ctx_len,
+                               self.n_acc, self.next_tok, self.committed, self.accept_ws, self.status)
+
     def launches_per_layer(self):
         """Our kernels per layer: append; for the tensor-core leg the query kernel and the verify
         kernel (the CUDA-core leg: the verify kernel); the split merge when the context is split,
@@ -258,18 +273,19 @@ class Step:
         split = self.ws.numel() > query_bytes
         return 1 + (2 if mma else 1) + (1 if split else 0)
 
-    def capture(self, **kw):
-        """The step's launches as one CUDA graph (no host launch gaps when replayed)."""
+    def capture(self, fn=None, **kw):
+        """The step's launches (or fn's) as one CUDA graph (no host launch gaps when replayed)."""
         torch = self.torch
+        fn = fn or (lambda: self.run(**kw))
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
-            self.run(**kw)                     # warm the launch path on the capture stream
+            fn()                               # warm the launch path on the capture stream
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            self.run(**kw)
+            fn()
         torch.cuda.synchronize()
         return graph
 
@@ -294,6 +310,7 @@ def run_ours(args, rank, world, local, pg):
     # the step, and its verify calls alone (for the per-launch roofline), as CUDA graphs
     g_step = st.capture()
     g_verify = st.capture(append=False)
+    g_accept = st.capture(st.accept)
     for _ in range(max(args.warmup, 3)):
         g_step.replay()
         g_verify.replay()
@@ -316,10 +333,17 @@ def run_ours(args, rank, world, local, pg):
         vev[s][0].record(stream)
         g_verify.replay()                   # the step's Ly verify calls back to back
         vev[s][1].record(stream)
+    aev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for s in range(args.steps):
+        flush.zero_()
+        aev[s][0].record(stream)
+        g_accept.replay()                   # the step's acceptance (argmax + acceptance kernels)
+        aev[s][1].record(stream)
     torch.cuda.synchronize()
     clock_info = clocks.stop()
     barrier(pg)
     step_ms = [a.elapsed_time(b_) for a, b_ in ev]
+    accept_us = statistics.mean(a.elapsed_time(b_) for a, b_ in aev) * 1e3
     verify_ms = [a.elapsed_time(b_) / Ly for a, b_ in vev for _ in range(Ly)]   # per verify call
     total_s = max_over_ranks(pg, sum(step_ms) / 1e3)
     assert int(st.status.item()) == 0, "device status flagged during the benchmark"
@@ -389,6 +413,9 @@ def run_ours(args, rank, world, local, pg):
                      "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": kv_bytes,
                      "mean_launch_us": mean_verify_s * 1e6},
+        "accept": {"us": accept_us, "vocab": st.vocab, "logits_bytes": st.rows * st.vocab * 2,
+                   "gbs": st.rows * st.vocab * 2 / (accept_us * 1e-6) / 1e9,
+                   "kernel": "q3kv_accept_greedy (argmax + acceptance kernels), bf16 logits, once per step"},
         "clocks": clock_info,
         "gpu_launches": args.steps * Ly * st.launches_per_layer(),
         "e2e": e2e,

@@ -64,14 +64,26 @@ __global__ void __launch_bounds__(kArgThreads) argmax_kernel(AcceptArgs a) {
         // chunk_elems is a multiple of kVec and the rows are 16-byte aligned
         const uint4* p = reinterpret_cast<const uint4*>(lg + c0);
         const int64_t n = (c1 - c0) / kVec;
-        for (int64_t k = threadIdx.x; k < n; k += kArgThreads) {
-            const uint4 u = __ldcs(p + k);
-            const T* e = reinterpret_cast<const T*>(&u);
+        constexpr int kUnroll = 4;                  // a thread's loads are all in flight at once
+        for (int64_t k0 = threadIdx.x; k0 < n; k0 += kUnroll * kArgThreads) {
+            uint4 u[kUnroll];
 #pragma unroll
-            for (int m = 0; m < kVec; ++m) {
-                const float v = to_f(e[m]);
-                nan |= (v != v);
-                if (v > b.v) { b.v = v; b.i = (int)(c0 + k * kVec + m); }   // ascending per thread: first max kept
+            for (int r = 0; r < kUnroll; ++r) {
+                const int64_t k = k0 + (int64_t)r * kArgThreads;
+                u[r] = k < n ? __ldcs(p + k) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int r = 0; r < kUnroll; ++r) {
+                const int64_t k = k0 + (int64_t)r * kArgThreads;
+                if (k >= n) break;
+                const T* e = reinterpret_cast<const T*>(&u[r]);
+#pragma unroll
+                for (int m = 0; m < kVec; ++m) {
+                    const float v = to_f(e[m]);
+                    nan |= (v != v);
+                    // ascending per thread: the first of equal maxima is kept
+                    if (beats(v, (int)(c0 + k * kVec + m), b.v, b.i)) { b.v = v; b.i = (int)(c0 + k * kVec + m); }
+                }
             }
         }
         for (int64_t k = c0 + n * kVec + threadIdx.x; k < c1; k += kArgThreads) {   // ragged tail
@@ -83,7 +95,7 @@ __global__ void __launch_bounds__(kArgThreads) argmax_kernel(AcceptArgs a) {
         for (int64_t k = c0 + threadIdx.x; k < c1; k += kArgThreads) {
             const float v = to_f(lg[k]);
             nan |= (v != v);
-            if (v > b.v) { b.v = v; b.i = (int)k; }
+            if (beats(v, (int)k, b.v, b.i)) { b.v = v; b.i = (int)k; }
         }
     }
     b = warp_best(b);
@@ -117,28 +129,34 @@ __global__ void __launch_bounds__(32) accept_kernel(AcceptArgs a) {
         return;
     }
     const int r0 = a.q_offsets[b];
-    int g[kMaxNq];
+    // every load up front: lane j < T holds query token j; lane k reduces
+    // chunks k, k + 32, .. of all T rows at once
+    const int tok = lane < T ? a.tokens[r0 + lane] : -1;
+    const float2* pp = reinterpret_cast<const float2*>(a.partial) + (int64_t)r0 * a.num_chunks;
+    Best c[kMaxNq];
 #pragma unroll
-    for (int j = 0; j < kMaxNq; ++j) {
-        g[j] = -1;
-        if (j < T) {
-            const float2* pp = reinterpret_cast<const float2*>(a.partial) + (int64_t)(r0 + j) * a.num_chunks;
-            Best c{-CUDART_INF_F, INT32_MAX};
-            for (int k = lane; k < a.num_chunks; k += 32) {
-                const float2 u = pp[k];
-                if (beats(u.x, __float_as_int(u.y), c.v, c.i)) { c.v = u.x; c.i = __float_as_int(u.y); }
+    for (int j = 0; j < kMaxNq; ++j) c[j] = Best{-CUDART_INF_F, INT32_MAX};
+    for (int k = lane; k < a.num_chunks; k += 32) {
+#pragma unroll
+        for (int j = 0; j < kMaxNq; ++j)
+            if (j < T) {
+                const float2 u = pp[(int64_t)j * a.num_chunks + k];
+                if (beats(u.x, __float_as_int(u.y), c[j].v, c[j].i)) { c[j].v = u.x; c[j].i = __float_as_int(u.y); }
             }
-            c = warp_best(c);
-            g[j] = c.i;
-        }
     }
-    if (lane == 0) {
-        int acc = 0;
-        while (acc < T - 1 && a.tokens[r0 + acc + 1] == g[acc]) ++acc;
-        int nxt = g[0];
+    int g_lane = -1;                                 // lane j: g_j
 #pragma unroll
-        for (int j = 1; j < kMaxNq; ++j)
-            if (j == acc) nxt = g[j];
+    for (int j = 0; j < kMaxNq; ++j)
+        if (j < T) {
+            const Best w = warp_best(c[j]);
+            if (lane == j) g_lane = w.i;
+        }
+    // drafts accepted while d_{j+1} == g_j: the first lane j < T-1 that differs ends the chain
+    const int next_tok = __shfl_down_sync(0xffffffffu, tok, 1);
+    const unsigned miss = __ballot_sync(0xffffffffu, lane < T - 1 && next_tok != g_lane);
+    const int acc = miss ? __ffs(miss) - 1 : T - 1;
+    const int nxt = __shfl_sync(0xffffffffu, g_lane, acc);
+    if (lane == 0) {
         a.n_accepted[b] = acc;
         a.next_token[b] = nxt;
         a.committed_len[b] = L - (T - 1 - acc);
