@@ -32,8 +32,8 @@
 // Issue rate, not the tensor pipe, limits small-N MMAs on this GPU: one thread
 // issues a K=16 MMA about every 54 cycles, while an M=128, N=48 MMA executes
 // in about 24.  So four warps issue, each into its own accumulator and each
-// waiting only for its own operands: QK over dims 0..127 into S_a and over
-// 128..255 into S_b (summed by the softmax), PV into the two 128-dim halves of
+// waiting only for its own operands: QK over dims 0..127 into S, then (after
+// those MMAs completed) over dims 128..255 onto S, PV into the two 128-dim halves of
 // O^T.  Every MMA sequence is fully unrolled, its descriptors formed by
 // constant offsets.
 //
@@ -44,12 +44,13 @@
 // the loop, and the dequantising warps hold no prefetch registers.
 //
 // Warp roles (16 warps), handing tiles on with mbarriers:
-//   A   warps 0-3   softmax: thread = position; reads S_a + S_b from TMEM;
+//   A   warps 0-3   softmax: thread = position; reads S from TMEM;
 //                   scores are in log2 units and the running row maximum is
 //                   only raised when a score exceeds it by more than 8 (then l
 //                   and the O^T columns are rescaled), so most tiles need no
 //                   cross-lane maximum; P = 2^(s - m) <= 256 goes to shared
-//                   memory as fp16 hi/lo; row sums by a transposing butterfly.
+//                   memory as fp16 hi/lo; row sums accumulate per lane in TMEM
+//                   and are reduced across lanes once, after the last tile.
 //   B1  warps 4-7   thread = position: its K record from shared memory, K_hat
 //                   into TMEM in two halves (dims 0..127, 128..255), each as
 //                   soon as the QK half of the previous tile has read it.
@@ -58,7 +59,7 @@
 //                   every sub-tile.
 //   MQa, MQb  warps 12-13   one thread each issues a QK half
 //   MP0, MP1  warps 14-15   one thread each issues the PV of an O^T half
-// TMEM (512 columns): K_hat hi | K_hat lo | S_a | S_b | O^T dims 0..127 | 128..255.
+// TMEM (512 columns): K_hat hi | K_hat lo | S | row-sum partials | O^T dims 0..127 | 128..255.
 //
 // After the last tile the A warps read O^T (thread = two output dims) and
 // either finish the rows (one split: divide by l, rotate back by H) or store
@@ -100,8 +101,8 @@ constexpr float kMaxScale = 5696.0f;        // 11.5 * s must stay below the fp16
 // TMEM columns (allocation of 512)
 constexpr uint32_t kColKHi = 0;
 constexpr uint32_t kColKLo = 128;
-constexpr uint32_t kColSa = 256;            // S^T over dims 0..127
-constexpr uint32_t kColSb = 320;            // S^T over dims 128..255
+constexpr uint32_t kColS = 256;             // S^T (QK over dims 0..127, then 128..255)
+constexpr uint32_t kColL = 320;             // row-sum partials: lane = position slot, column = row
 constexpr uint32_t kColO0 = 384;
 constexpr uint32_t kColO1 = 448;
 constexpr uint32_t kTmemCols = 512;
@@ -112,7 +113,7 @@ constexpr int kBarA = 1;                    // the 128 softmax threads
 struct Bars {
     unsigned long long vfull[4][2]; // V records of B2 warp q's sub-tile q + 4e landed
     unsigned long long kready[2];   // K_hat dims half in TMEM (4 B1 warps)
-    unsigned long long qk_done[2];  // S_a / S_b written, that K_hat half read (1 commit)
+    unsigned long long qk_done[2];  // QK half h done (S complete after half 1), that K_hat half read
     unsigned long long s_free;      // S read (4 A warps)
     unsigned long long q_ready;     // Q hi/lo copied in (bulk copy bytes)
     unsigned long long p_ready[2];  // P^T buffer b stored, O^T rescaled (4 A warps)
@@ -660,26 +661,16 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         bool ok = true;
         for (int i = 0; i < n_tiles; ++i) {
             const int pb = i & 1;                       // P^T buffer of this tile
-            ok = ok && mbar_wait(&bar.qk_done[0], (uint32_t)(i & 1), abort);
+            // the second QK half is issued only after the first one completed,
+            // so its commit covers the whole S
             ok = ok && mbar_wait(&bar.qk_done[1], (uint32_t)(i & 1), abort);
             tc_fence_after();
-            // S = S_a + S_b, 32 columns per TMEM round trip; columns >= N are -inf
+            // S, in one TMEM round trip; columns >= N are -inf
             float x[kRows];
 #pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-                if (32 * c2 < N) {
-                    float y[32];
-                    tmem_ld16(tmem + lane_base + kColSa + 32 * c2, &x[32 * c2]);
-                    tmem_ld16(tmem + lane_base + kColSb + 32 * c2, &y[0]);
-                    if (32 * c2 + 16 < N) {
-                        tmem_ld16(tmem + lane_base + kColSa + 32 * c2 + 16, &x[32 * c2 + 16]);
-                        tmem_ld16(tmem + lane_base + kColSb + 32 * c2 + 16, &y[16]);
-                    }
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) x[32 * c2 + k] += y[k];
-                }
-            }
+            for (int c = 0; c < 4; ++c)
+                if (16 * c < N) tmem_ld16(tmem + lane_base + kColS + 16 * c, &x[16 * c]);
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.s_free);
@@ -728,7 +719,6 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                     const float al = exp2f(m_old - m_new);
                     sm.m_run[tid] = m_new;
                     sm.thr[tid] = m_new + kRescaleThreshold;
-                    sm.l_run[tid] *= al;
                     sm.alpha[tid] = al;
                 }
                 named_sync(kBarA, 128);
@@ -748,8 +738,8 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                 ok = ok && mbar_wait(&bar.pv_done[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1), abort);
                 tc_fence_after();
 #pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t col = h ? kColO1 : kColO0;
+                for (int h = 0; h < 3; ++h) {           // O^T halves and the row-sum partials
+                    const uint32_t col = h == 0 ? kColO0 : (h == 1 ? kColO1 : kColL);
 #pragma unroll 1
                     for (int c = 0; c < N; c += 8) {
                         float v8[8];
@@ -787,11 +777,45 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.p_ready[pb]);
-            // row sums of this tile
-            sm.red[q][lane] = transpose_reduce<false>(*reinterpret_cast<float(*)[32]>(&x[0]));
-            if (N > 32) sm.red[q][32 + lane] = transpose_reduce<false>(*reinterpret_cast<float(*)[32]>(&x[32]));
+            // row sums: this thread's P values added to its lane's TMEM partials
+            // (the cross-lane sum is taken once, after the last tile)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (16 * c < N) {
+                    uint32_t u16[16];
+                    if (i > 0) {
+                        float y[16];
+                        tmem_ld16(tmem + lane_base + kColL + 16 * c, y);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) u16[k] = __float_as_uint(y[k] + x[16 * c + k]);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) u16[k] = __float_as_uint(x[16 * c + k]);
+                    }
+                    tmem_st16(tmem + lane_base + kColL + 16 * c, u16);
+                }
+            }
+            tmem_st_wait();
+        }
+        // l = column sums of the row-sum partials over the 128 lanes
+        {
+            float y[kRows];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (16 * c < N) tmem_ld16(tmem + lane_base + kColL + 16 * c, &y[16 * c]);
+                else
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) y[16 * c + k] = 0.0f;
+            }
+            tmem_ld_wait();
+            if (n_tiles == 0)
+#pragma unroll
+                for (int k = 0; k < kRows; ++k) y[k] = 0.0f;
+            sm.red[q][lane] = transpose_reduce<false>(*reinterpret_cast<float(*)[32]>(&y[0]));
+            if (N > 32) sm.red[q][32 + lane] = transpose_reduce<false>(*reinterpret_cast<float(*)[32]>(&y[32]));
             named_sync(kBarA, 128);
-            if (tid < N) sm.l_run[tid] += (sm.red[0][tid] + sm.red[1][tid]) + (sm.red[2][tid] + sm.red[3][tid]);
+            if (tid < N) sm.l_run[tid] = (sm.red[0][tid] + sm.red[1][tid]) + (sm.red[2][tid] + sm.red[3][tid]);
         }
         named_sync(kBarA, 128);   // l_run complete
         // ---- epilogue: O^T -> partial or finished rows
@@ -955,17 +979,20 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                 if (pend[e] >= 0) mbar_drain(&bar.vfull[q][e], (uint32_t)(pend[e] & 1));
     } else if (warp < 14) {
         // ================================================================ MQa / MQb: QK halves
-        const int h = warp - 12;                     // 0: dims 0..127 -> S_a, 1: dims 128..255 -> S_b
+        const int h = warp - 12;                     // 0: dims 0..127, 1: dims 128..255 (both into S)
         const uint32_t idesc_qk = make_idesc(N, false, false);
         const uint64_t bq_hi = make_desc(smem_u32(sm.qhi) + h * 8 * 256, kQLbo, kQSbo);
         const uint64_t bq_lo = make_desc(smem_u32(sm.qlo) + h * 8 * 256, kQLbo, kQSbo);
-        const uint32_t dS = tmem + (h ? kColSb : kColSa);
+        const uint32_t dS = tmem + kColS;
         const uint32_t aK_hi = tmem + kColKHi + 64 * h;
         const uint32_t aK_lo = tmem + kColKLo + 64 * h;
         bool qok = warp_wait(&bar.q_ready, 0u, abort);
         for (int i = 0; qok && i < n_tiles; ++i) {
             if (!warp_wait(&bar.kready[h], (uint32_t)(i & 1), abort)) break;
-            if (i >= 1 && !warp_wait(&bar.s_free, (uint32_t)((i - 1) & 1), abort)) break;
+            // half 0 overwrites S once the softmax has read the previous tile's;
+            // half 1 accumulates onto it after half 0's MMAs have completed
+            if (h == 0 && i >= 1 && !warp_wait(&bar.s_free, (uint32_t)((i - 1) & 1), abort)) break;
+            if (h == 1 && !warp_wait(&bar.qk_done[0], (uint32_t)(i & 1), abort)) break;
             tc_fence_after();
             // descriptors are formed by the whole (converged) warp, so they stay
             // warp-uniform; one elected lane issues
@@ -973,7 +1000,7 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
             for (int j = 0; j < 8; ++j) {   // descriptor start address is in 16-byte units
                 const uint64_t ko = (uint64_t)(16 * j);
                 if (elect_one()) {
-                    mma_ts(dS, aK_hi + 8 * j, bq_hi + ko, idesc_qk, j > 0 ? 1u : 0u);
+                    mma_ts(dS, aK_hi + 8 * j, bq_hi + ko, idesc_qk, (h == 0 && j == 0) ? 0u : 1u);
                     mma_ts(dS, aK_hi + 8 * j, bq_lo + ko, idesc_qk, 1u);
                     mma_ts(dS, aK_lo + 8 * j, bq_hi + ko, idesc_qk, 1u);
                 }
