@@ -62,3 +62,85 @@ def greedy_accept(logits: np.ndarray, q_offsets, n_q, tokens, ctx_len):
         nxt[b] = g[a]
         committed[b] = int(ctx_len[b]) - (T - 1 - a)
     return n_acc, nxt, committed
+
+
+# ----------------------------------------------------------------------------- sampled acceptance
+# The pages' sampled speculative decode ("Model tool protocol" bullet: Gumbel-max
+# sampling with rejection-sampled acceptance, seeded and reproducible; greedy
+# unchanged).  Reading taken here (the top-p nucleus filter is not modelled):
+#
+# * target distribution of row j: p_j = softmax(logits_j / tau);
+# * the drafts are point masses (a deterministic drafter), so draft d_{j+1} is
+#   accepted with probability min(1, p_j(d)/1) = p_j(d): accepted iff the
+#   given uniform u_j (one per row, passed in) is below p_j(d_{j+1});
+# * at the first rejection (row a) the replacement is drawn from the residual
+#   max(0, p_a - delta_d) / norm, i.e. p_a without the rejected token, by
+#   Gumbel-max over the other tokens; if every draft is accepted the bonus token
+#   is drawn from p_{T-1} the same way;
+# * Gumbel noise G(row, x) = -log(-log U) with U from a counter-based
+#   SplitMix64 stream (published definition: state += 0x9E3779B97F4A7C15, then
+#   the 64-bit mix below): U = ((z >> 40) + 0.5) / 2^24 with z the output of
+#   counter k = row * 2^32 + x of the stream seeded with `seed`.
+
+MASK64 = (1 << 64) - 1
+GOLDEN_GAMMA = 0x9E3779B97F4A7C15
+
+
+def splitmix64_at(seed: int, k: int) -> int:
+    """Output number k (0-based) of the SplitMix64 stream seeded with `seed`."""
+    z = (seed + (k + 1) * GOLDEN_GAMMA) & MASK64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & MASK64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & MASK64
+    return z ^ (z >> 31)
+
+
+def noise_uniform(seed: int, row: int, tokens: np.ndarray) -> np.ndarray:
+    """U(row, x) in (0, 1) for the given token ids (exact 24-bit values, float64)."""
+    tokens = np.asarray(tokens, np.uint64)
+    with np.errstate(over="ignore"):
+        k = np.uint64(row) * np.uint64(1 << 32) + tokens
+        z = np.uint64(seed) + (k + np.uint64(1)) * np.uint64(GOLDEN_GAMMA)
+        z = (z ^ (z >> np.uint64(30))) * np.uint64(0xBF58476D1CE4E5B9)
+        z = (z ^ (z >> np.uint64(27))) * np.uint64(0x94D049BB133111EB)
+        z = z ^ (z >> np.uint64(31))
+    return ((z >> np.uint64(40)).astype(np.float64) + 0.5) / float(1 << 24)
+
+
+def gumbel_keys(logits_row: np.ndarray, tau: float, seed: int, row: int) -> np.ndarray:
+    """logit / tau + G(row, x) for every token x (float64)."""
+    x = np.arange(logits_row.shape[0])
+    return np.asarray(logits_row, np.float64) / tau - np.log(-np.log(noise_uniform(seed, row, x)))
+
+
+def target_prob(logits_row: np.ndarray, tau: float, token: int) -> float:
+    """p(token) under softmax(logits_row / tau), float64."""
+    l = np.asarray(logits_row, np.float64) / tau
+    m = l.max()
+    e = np.exp(l - m)
+    return float(e[token] / e.sum()) if 0 <= token < l.shape[0] else 0.0
+
+
+def sample_accept(logits: np.ndarray, q_offsets, n_q, tokens, ctx_len, tau: float, uniforms, seed: int):
+    """Rejection-sampled acceptance for every slot; returns (n_accepted, next_token, committed_len)."""
+    S = len(n_q)
+    n_acc = np.zeros(S, np.int32)
+    nxt = np.full(S, -1, np.int32)
+    committed = np.array(ctx_len, np.int64).astype(np.int32)
+    V = logits.shape[1]
+    for b in range(S):
+        T = int(n_q[b])
+        if T <= 0:
+            continue
+        r0 = int(q_offsets[b])
+        a = 0
+        while a < T - 1 and float(uniforms[r0 + a]) < target_prob(logits[r0 + a], tau, int(tokens[r0 + a + 1])):
+            a += 1
+        keys = gumbel_keys(logits[r0 + a], tau, seed, r0 + a)
+        if a < T - 1:                                  # residual: the rejected token is excluded
+            d = int(tokens[r0 + a + 1])
+            if 0 <= d < V:
+                keys[d] = -np.inf
+        n_acc[b] = a
+        nxt[b] = int(np.argmax(keys))
+        committed[b] = int(ctx_len[b]) - (T - 1 - a)
+    return n_acc, nxt, committed

@@ -98,3 +98,65 @@ def test_invariants_random():
         assert a[b] == want_a[b]
         assert nxt[b] == g[offs[b] + a[b]]
         assert com[b] == ctx[b] - (T - 1 - a[b])
+
+
+# ----------------------------------------------------------------------------- sampled acceptance
+from oracle.accept import gumbel_keys, noise_uniform, sample_accept, splitmix64_at, target_prob
+
+
+def test_splitmix64_published_outputs():
+    # the reference generator's first outputs for seed 0
+    assert splitmix64_at(0, 0) == 0xE220A8397B1DCDAF
+    assert splitmix64_at(0, 1) == 0x6E789E6AA1B965F4
+    assert splitmix64_at(0, 2) == 0x06C45D188009454F
+
+
+def test_noise_uniform_matches_scalar_definition():
+    seed, row = 12345, 7
+    toks = np.array([0, 1, 2, 1000, 248319])
+    got = noise_uniform(seed, row, toks)
+    for t, g in zip(toks, got):
+        z = splitmix64_at(seed, row * (1 << 32) + int(t))
+        assert g == ((z >> 40) + 0.5) / (1 << 24)
+    assert np.all((got > 0) & (got < 1))
+
+
+def test_two_token_hand_case():
+    # logits (0, ln 3), tau 1: p(token 1) = 3/4; the residual after rejecting
+    # token 1 has one token left, so the replacement is 0 whatever the noise
+    lg = np.array([[0.0, np.log(3.0)], [5.0, 0.0]])
+    assert abs(target_prob(lg[0], 1.0, 1) - 0.75) < 1e-15
+    a, nxt, com = sample_accept(lg, [0], [2], np.array([0, 1]), [9], 1.0, np.array([0.70, 0.5]), seed=3)
+    assert int(a[0]) == 1 and int(com[0]) == 9            # accepted; bonus drawn from row 1
+    a, nxt, com = sample_accept(lg, [0], [2], np.array([0, 1]), [9], 1.0, np.array([0.80, 0.5]), seed=3)
+    assert (int(a[0]), int(nxt[0]), int(com[0])) == (0, 0, 8)
+
+
+def test_gumbel_max_samples_the_softmax():
+    # empirical frequencies of argmax(logit/tau + G) over many independent rows
+    lg = np.array([1.0, 0.0, -1.0, 2.0, 0.5])
+    tau = 0.7
+    n = 40000
+    counts = np.zeros(5)
+    for row in range(n):
+        counts[int(np.argmax(gumbel_keys(lg, tau, 99, row)))] += 1
+    p = np.exp(lg / tau - (lg / tau).max())
+    p /= p.sum()
+    assert np.max(np.abs(counts / n - p)) < 0.012
+
+
+def test_low_temperature_reduces_to_greedy():
+    rng = np.random.default_rng(4)
+    nq = [5, 1, 0, 7]
+    offs = np.concatenate([[0], np.cumsum(nq)[:-1]])
+    rows = sum(nq)
+    lg = rng.standard_normal((rows, 30))
+    g = lg.argmax(axis=1)
+    toks = rng.integers(0, 30, size=rows).astype(np.int32)
+    toks[1:3] = g[0:2]                                 # slot 0 accepts 2 drafts greedily
+    ctx = [50, 60, 70, 80]
+    u = rng.uniform(0.001, 0.999, size=rows)
+    want = greedy_accept(lg, offs, nq, toks, ctx)
+    got = sample_accept(lg, offs, nq, toks, ctx, 1e-4, u, seed=1)
+    for w_, g_ in zip(want, got):
+        assert np.array_equal(w_, g_)
