@@ -245,10 +245,39 @@ Q3KV_API int q3kv_verify_attn_noalloc(void* stream, const q3kv_cache_desc* desc,
  * T_b > ctx_len or rows past num_rows set Q3KV_STATUS_BAD_LENGTH and give the
  * slot (0, -1, ctx_len); a NaN logit sets Q3KV_STATUS_NONFINITE_INPUT (its
  * row's argmax is then unspecified).  Asynchronous on the stream. */
-Q3KV_API int q3kv_accept_workspace_bytes(int32_t num_rows, int32_t vocab, size_t* bytes);
+Q3KV_API int q3kv_accept_workspace_bytes(int32_t num_rows, int32_t vocab, size_t* bytes);   /* either call */
 Q3KV_API int q3kv_accept_greedy(void* stream, const void* logits, int32_t dtype, int32_t vocab,
                        const int32_t* d_q_offsets, const int32_t* d_n_q, const int32_t* d_tokens,
                        int32_t num_slots, int32_t num_rows, int32_t max_n_q, const int32_t* d_ctx_len,
+                       int32_t* d_n_accepted, int32_t* d_next_token, int32_t* d_committed_len,
+                       void* d_workspace, size_t workspace_bytes, int32_t* d_status);
+
+/* ---- sampled acceptance ------------------------------------------------------
+ * Source: "Quasar" (q27) wiki, "Model tool protocol" bullet: temperature > 0
+ * routes to sampled speculative decode with Gumbel-max sampling and
+ * rejection-sampled acceptance, seeded and reproducible.  This call's reading
+ * (the pages' top-p nucleus filter is not built): the drafts are point masses
+ * (a deterministic drafter), p_j = softmax(logits row j / temperature), and
+ *   draft d_{j+1} is accepted iff d_uniforms[row j] < p_j(d_{j+1});
+ *   at the first rejected row a, next = argmax over x != d_{a+1} of
+ *     logits_a[x] / temperature + G(row, x)   (a sample of p_a without the
+ *     rejected token, i.e. the residual of the rejection rule);
+ *   if every draft is accepted, next = the same argmax over all x of the last
+ *     row (the bonus token);
+ *   G(row, x) = -log(-log U), U = ((z >> 41) + 0.5) / 2^23, z = output number
+ *     row * 2^32 + x of the SplitMix64 stream seeded with `seed` (rows are
+ *     global logits rows).
+ * Same arguments, outputs, workspace and errors as q3kv_accept_greedy, plus:
+ *   temperature  > 0 and finite (else Q3KV_ERR_INVALID_ARG)
+ *   d_uniforms   device float [num_rows], values in [0, 1): row j's uniform
+ *                tests the draft that follows query token j (the caller draws
+ *                them; the last row of a slot is unused)
+ * The probabilities and keys are computed in float32; results equal the float64
+ * definition except where a uniform or a key lies within rounding of a tie. */
+Q3KV_API int q3kv_accept_sample(void* stream, const void* logits, int32_t dtype, int32_t vocab,
+                       const int32_t* d_q_offsets, const int32_t* d_n_q, const int32_t* d_tokens,
+                       int32_t num_slots, int32_t num_rows, int32_t max_n_q, const int32_t* d_ctx_len,
+                       float temperature, const float* d_uniforms, uint64_t seed,
                        int32_t* d_n_accepted, int32_t* d_next_token, int32_t* d_committed_len,
                        void* d_workspace, size_t workspace_bytes, int32_t* d_status);
 

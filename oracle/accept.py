@@ -79,8 +79,9 @@ def greedy_accept(logits: np.ndarray, q_offsets, n_q, tokens, ctx_len):
 #   is drawn from p_{T-1} the same way;
 # * Gumbel noise G(row, x) = -log(-log U) with U from a counter-based
 #   SplitMix64 stream (published definition: state += 0x9E3779B97F4A7C15, then
-#   the 64-bit mix below): U = ((z >> 40) + 0.5) / 2^24 with z the output of
-#   counter k = row * 2^32 + x of the stream seeded with `seed`.
+#   the 64-bit mix below): U = ((z >> 41) + 0.5) / 2^23 (exact in float32 and
+#   float64) with z the output of counter k = row * 2^32 + x of the stream
+#   seeded with `seed`.
 
 MASK64 = (1 << 64) - 1
 GOLDEN_GAMMA = 0x9E3779B97F4A7C15
@@ -103,7 +104,7 @@ def noise_uniform(seed: int, row: int, tokens: np.ndarray) -> np.ndarray:
         z = (z ^ (z >> np.uint64(30))) * np.uint64(0xBF58476D1CE4E5B9)
         z = (z ^ (z >> np.uint64(27))) * np.uint64(0x94D049BB133111EB)
         z = z ^ (z >> np.uint64(31))
-    return ((z >> np.uint64(40)).astype(np.float64) + 0.5) / float(1 << 24)
+    return ((z >> np.uint64(41)).astype(np.float64) + 0.5) / float(1 << 23)
 
 
 def gumbel_keys(logits_row: np.ndarray, tau: float, seed: int, row: int) -> np.ndarray:

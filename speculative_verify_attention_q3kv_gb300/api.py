@@ -164,3 +164,20 @@ def accept_greedy(logits: torch.Tensor, q_offsets: torch.Tensor, n_q: torch.Tens
                                         _ptr(n_accepted), _ptr(next_token), _ptr(committed_len), _ptr(workspace),
                                         nbytes, _ptr(status))
     check(rc, "q3kv_accept_greedy")
+
+
+def accept_sample(logits: torch.Tensor, q_offsets: torch.Tensor, n_q: torch.Tensor, tokens: torch.Tensor,
+                  max_n_q: int, ctx_len: torch.Tensor, temperature: float, uniforms: torch.Tensor, seed: int,
+                  n_accepted: torch.Tensor, next_token: torch.Tensor, committed_len: torch.Tensor,
+                  workspace: Optional[torch.Tensor], status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """q3kv_accept_sample: rejection-sampled acceptance; uniforms float32 [rows]."""
+    rows, vocab = logits.shape
+    if uniforms.dtype != torch.float32:
+        raise TypeError("uniforms must be float32")
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = _lib.load().q3kv_accept_sample(_stream(stream), _ptr(logits), _dtype_code(logits), vocab, _ptr(q_offsets),
+                                        _ptr(n_q), _ptr(tokens), n_q.shape[0], rows, max_n_q, _ptr(ctx_len),
+                                        float(temperature), _ptr(uniforms), int(seed) & ((1 << 64) - 1),
+                                        _ptr(n_accepted), _ptr(next_token), _ptr(committed_len), _ptr(workspace),
+                                        nbytes, _ptr(status))
+    check(rc, "q3kv_accept_sample")

@@ -163,6 +163,147 @@ __global__ void __launch_bounds__(32) accept_kernel(AcceptArgs a) {
     }
 }
 
+// ---------------------------------------------------------------- sampled acceptance
+// Reading of the pages' sampled speculative decode (Gumbel-max sampling with
+// rejection-sampled acceptance; the top-p nucleus filter is not built): drafts
+// are point masses, so d_{j+1} is accepted iff u_j < p_j(d_{j+1}) with
+// p_j = softmax(logits_j / tau); at the first rejection (row a) the next token
+// is argmax over x != d_{a+1} of logits_a[x] / tau + G(a, x), else the argmax
+// over all x of the last row's keys.  G = -log(-log U), U from the counter-based
+// SplitMix64 stream: U = ((z >> 41) + 0.5) / 2^23 with z output number
+// row * 2^32 + x of the stream seeded with `seed`.
+
+__device__ __forceinline__ float noise_uniform(uint64_t seed, uint32_t row, uint32_t x) {
+    const uint64_t k = ((uint64_t)row << 32) + x;
+    uint64_t z = seed + (k + 1ull) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    return ((float)(uint32_t)(z >> 41) + 0.5f) * (1.0f / 8388608.0f);
+}
+
+// Per (row, chunk): online (max, sum of exp) of logits / tau, and the best
+// Gumbel key overall and without the row's next query token.
+struct SampleStat {
+    float m, s;
+    float k1;
+    int i1;
+    float k2;
+    int i2;
+};
+
+__device__ __forceinline__ SampleStat stat_merge(SampleStat a, SampleStat b) {
+    SampleStat r;
+    r.m = fmaxf(a.m, b.m);
+    r.s = (a.m == -CUDART_INF_F ? 0.0f : a.s * __expf(a.m - r.m)) + (b.m == -CUDART_INF_F ? 0.0f : b.s * __expf(b.m - r.m));
+    const bool b1 = beats(b.k1, b.i1, a.k1, a.i1);
+    r.k1 = b1 ? b.k1 : a.k1;
+    r.i1 = b1 ? b.i1 : a.i1;
+    const bool b2 = beats(b.k2, b.i2, a.k2, a.i2);
+    r.k2 = b2 ? b.k2 : a.k2;
+    r.i2 = b2 ? b.i2 : a.i2;
+    return r;
+}
+
+__device__ __forceinline__ SampleStat stat_warp(SampleStat v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        SampleStat w;
+        w.m = __shfl_xor_sync(0xffffffffu, v.m, o);
+        w.s = __shfl_xor_sync(0xffffffffu, v.s, o);
+        w.k1 = __shfl_xor_sync(0xffffffffu, v.k1, o);
+        w.i1 = __shfl_xor_sync(0xffffffffu, v.i1, o);
+        w.k2 = __shfl_xor_sync(0xffffffffu, v.k2, o);
+        w.i2 = __shfl_xor_sync(0xffffffffu, v.i2, o);
+        v = stat_merge(v, w);
+    }
+    return v;
+}
+
+__device__ __forceinline__ SampleStat stat_empty() {
+    return SampleStat{-CUDART_INF_F, 0.0f, -CUDART_INF_F, INT32_MAX, -CUDART_INF_F, INT32_MAX};
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kArgThreads) sample_stats_kernel(AcceptArgs a) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __shared__ SampleStat red[kArgThreads / 32];
+    const int row = blockIdx.y, chunk = blockIdx.x;
+    const int64_t c0 = (int64_t)chunk * a.chunk_elems;
+    const int64_t c1 = min((int64_t)a.vocab, c0 + a.chunk_elems);
+    const T* lg = static_cast<const T*>(a.logits) + (int64_t)row * a.vocab;
+    const int excl = row + 1 < a.num_rows ? a.tokens[row + 1] : -1;
+    SampleStat st = stat_empty();
+    bool nan = false;
+    for (int64_t k = c0 + threadIdx.x; k < c1; k += kArgThreads) {
+        const float l = to_f(lg[k]) * a.inv_tau;
+        nan |= (l != l);
+        // running max and sum of exp(l - max)
+        if (l > st.m) {
+            st.s = (st.m == -CUDART_INF_F ? 0.0f : st.s * __expf(st.m - l)) + 1.0f;
+            st.m = l;
+        } else {
+            st.s += __expf(l - st.m);
+        }
+        const float key = l - logf(-logf(noise_uniform(a.seed, (uint32_t)row, (uint32_t)k)));
+        if (beats(key, (int)k, st.k1, st.i1)) { st.k1 = key; st.i1 = (int)k; }
+        if ((int)k != excl && beats(key, (int)k, st.k2, st.i2)) { st.k2 = key; st.i2 = (int)k; }
+    }
+    st = stat_warp(st);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = st;
+    if (__any_sync(0xffffffffu, nan) && (threadIdx.x & 31) == 0 && a.status)
+        atomicOr(a.status, Q3KV_STATUS_NONFINITE_INPUT);
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        SampleStat c = threadIdx.x < kArgThreads / 32 ? red[threadIdx.x] : stat_empty();
+        c = stat_warp(c);
+        if (threadIdx.x == 0) reinterpret_cast<SampleStat*>(a.partial)[(int64_t)row * a.num_chunks + chunk] = c;
+    }
+}
+
+template <typename TIn>
+__global__ void __launch_bounds__(32) sample_accept_kernel(AcceptArgs a) {
+    const int b = blockIdx.x, lane = threadIdx.x;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int T = a.n_q[b];
+    const int32_t L = a.ctx_len[b];
+    if (T <= 0 || T > a.max_n_q || T > L || a.q_offsets[b] < 0 || a.q_offsets[b] + T > a.num_rows) {
+        if (lane == 0) {
+            if (T != 0 && a.status) atomicOr(a.status, Q3KV_STATUS_BAD_LENGTH);
+            a.n_accepted[b] = 0;
+            a.next_token[b] = -1;
+            a.committed_len[b] = L;
+        }
+        return;
+    }
+    const int r0 = a.q_offsets[b];
+    // lane j < T: row j's statistics (lanes reduce the chunks together), its
+    // draft test and its two candidates
+    const int tok_next = lane + 1 < T ? a.tokens[r0 + lane + 1] : -1;
+    const float u = lane < T ? a.uniforms[r0 + lane] : 1.0f;
+    const float l_d = (lane + 1 < T && tok_next >= 0 && tok_next < a.vocab)
+                          ? to_f(static_cast<const TIn*>(a.logits)[(int64_t)(r0 + lane) * a.vocab + tok_next]) * a.inv_tau
+                          : -CUDART_INF_F;
+    const SampleStat* pp = reinterpret_cast<const SampleStat*>(a.partial) + (int64_t)r0 * a.num_chunks;
+    SampleStat mine = stat_empty();
+    for (int j = 0; j < T; ++j) {
+        SampleStat c = stat_empty();
+        for (int k = lane; k < a.num_chunks; k += 32) c = stat_merge(c, pp[(int64_t)j * a.num_chunks + k]);
+        c = stat_warp(c);
+        if (lane == j) mine = c;
+    }
+    const float p = (lane + 1 < T) ? __expf(l_d - mine.m) / mine.s : 0.0f;
+    const unsigned miss = __ballot_sync(0xffffffffu, lane + 1 < T && !(u < p));
+    const int acc = miss ? __ffs(miss) - 1 : T - 1;
+    const int cand = (acc < T - 1) ? mine.i2 : mine.i1;            // residual sample, or the bonus token
+    const int nxt = __shfl_sync(0xffffffffu, cand, acc);
+    if (lane == 0) {
+        a.n_accepted[b] = acc;
+        a.next_token[b] = nxt;
+        a.committed_len[b] = L - (T - 1 - acc);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t stream) {
@@ -183,6 +324,31 @@ cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, accept_kernel, a);
+}
+
+}  // namespace q3kv
+
+namespace q3kv {
+
+cudaError_t launch_accept_sample(const AcceptArgs& a, cudaStream_t stream) {
+    if (a.num_rows > 0) {
+        const dim3 grid((unsigned)a.num_chunks, (unsigned)a.num_rows);
+        if (a.dtype == Q3KV_F32) sample_stats_kernel<float><<<grid, kArgThreads, 0, stream>>>(a);
+        else sample_stats_kernel<__nv_bfloat16><<<grid, kArgThreads, 0, stream>>>(a);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.num_slots);
+    cfg.blockDim = dim3(32);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (a.dtype == Q3KV_F32) return cudaLaunchKernelEx(&cfg, sample_accept_kernel<float>, a);
+    return cudaLaunchKernelEx(&cfg, sample_accept_kernel<__nv_bfloat16>, a);
 }
 
 }  // namespace q3kv

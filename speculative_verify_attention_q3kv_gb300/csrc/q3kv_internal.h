@@ -87,10 +87,16 @@ struct AcceptArgs {
     int32_t* n_accepted;
     int32_t* next_token;
     int32_t* committed_len;
-    void* partial;             // [num_rows, num_chunks] (max, index) pairs
+    void* partial;             // [num_rows, num_chunks] per-chunk results
     int32_t* status;
+    // sampled acceptance only
+    float inv_tau;             // 1 / temperature
+    const float* uniforms;     // [num_rows] draft-test uniforms
+    uint64_t seed;             // Gumbel noise stream
 };
+constexpr size_t kAcceptPartialBytes = 24;   // largest per-chunk record (sampled acceptance)
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t stream);
+cudaError_t launch_accept_sample(const AcceptArgs& a, cudaStream_t stream);
 
 // FMA (CUDA-core) leg: rows per CTA, and its workspace/launch.
 constexpr int kFmaRows = 64;

@@ -128,3 +128,86 @@ def test_step_accept_commit_then_next_step_overwrites_rejected_rows():
     q2 = qi.q_rows(w, 0, 0, 1, T2)
     out = c.verify(0, [int(com[0]) + T2], [T2], [q2], impl=2)
     check_close(out, oracle_verify(w, 0, 0, int(com[0]), q2, kk, vv))
+
+
+# ----------------------------------------------------------------------------- sampled acceptance
+from oracle.accept import gumbel_keys, sample_accept, target_prob
+
+
+def _run_sample(logits_np, offs, nq, toks, ctx, bf16, tau, u, seed):
+    from speculative_verify_attention_q3kv_gb300 import api
+    rows, vocab = logits_np.shape
+    lg = torch.from_numpy(logits_np).cuda()
+    if bf16:
+        lg = lg.to(torch.bfloat16)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    S = len(nq)
+    out = [torch.full((S,), -7, **i32) for _ in range(3)]
+    ws = torch.empty(max(api.accept_workspace_bytes(rows, vocab), 8), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, **i32)
+    api.accept_sample(lg, torch.tensor(np.asarray(offs, np.int32), **i32), torch.tensor(np.asarray(nq, np.int32), **i32),
+                      torch.tensor(np.asarray(toks, np.int32), **i32), max(nq),
+                      torch.tensor(np.asarray(ctx, np.int32), **i32), tau,
+                      torch.from_numpy(np.asarray(u, np.float32)).cuda(), seed, *out, ws, st)
+    torch.cuda.synchronize()
+    return [o.cpu().numpy() for o in out] + [int(st.item())]
+
+
+@pytest.mark.parametrize("vocab", [1000, 50_257, qi.VOCAB])
+@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("tau", [0.6, 1.0])
+def test_sample_accept_matches_oracle(vocab, bf16, tau):
+    rng = np.random.default_rng(vocab + int(10 * tau) + 3 * bf16)
+    nq = [int(x) for x in rng.integers(0, 17, size=8)]
+    nq[1], nq[5] = 0, 1
+    offs = np.concatenate([[0], np.cumsum(nq)[:-1]]).astype(np.int32)
+    rows = int(sum(nq))
+    logits = qi.logits_rows(vocab + 1, rows, vocab, "normal", bf16)
+    lg64 = logits.astype(np.float64)
+    # drafts drawn from each row's top tokens, so acceptance probabilities are sizeable
+    toks = qi.random_tokens(vocab, rows, vocab)
+    top = np.argsort(-lg64, axis=1)[:, :3]
+    for b, T in enumerate(nq):
+        for j in range(1, T):
+            toks[offs[b] + j] = top[offs[b] + j - 1, int(rng.integers(0, 3))]
+    # uniforms, kept clear of each draft test's boundary
+    u = rng.uniform(0.0, 1.0, size=rows)
+    for b, T in enumerate(nq):
+        for j in range(T - 1):
+            r = offs[b] + j
+            p = target_prob(lg64[r], tau, int(toks[r + 1]))
+            while abs(u[r] - p) < 2e-3:
+                u[r] = rng.uniform()
+    u = u.astype(np.float32)
+    ctx = [int(x) for x in rng.integers(20, 5000, size=8)]
+    seed = 0x1234_5678_9ABC_DEF0 + vocab
+    want = sample_accept(lg64, offs, nq, toks, ctx, tau, u.astype(np.float64), seed)
+    n_acc, nxt, com, st = _run_sample(logits, offs, nq, toks, ctx, bf16, tau, u, seed)
+    assert st == 0
+    assert np.array_equal(n_acc, want[0]) and np.array_equal(com, want[2])
+    for b, T in enumerate(nq):
+        if T == 0:
+            assert nxt[b] == -1
+            continue
+        if nxt[b] == want[1][b]:
+            continue
+        # a different token must still be a maximal Gumbel key up to rounding
+        r = offs[b] + int(n_acc[b])
+        keys = gumbel_keys(lg64[r], tau, seed, r)
+        if n_acc[b] < T - 1:
+            keys[int(toks[r + 1])] = -np.inf
+        assert keys[nxt[b]] >= keys.max() - 1e-4, (b, nxt[b], want[1][b])
+
+
+def test_sample_accept_low_temperature_is_greedy():
+    vocab = 4099
+    nq = [6, 3, 1]
+    offs = [0, 6, 9]
+    logits = qi.logits_rows(11, 10, vocab)
+    toks = _plant(logits, offs, nq, [3, 2, 0], 11, vocab)
+    ctx = [100, 50, 7]
+    u = np.random.default_rng(2).uniform(0.01, 0.99, size=10).astype(np.float32)
+    want = greedy_accept(logits.astype(np.float64), offs, nq, toks, ctx)
+    n_acc, nxt, com, st = _run_sample(logits, offs, nq, toks, ctx, False, 1e-3, u, 5)
+    assert st == 0
+    assert np.array_equal(n_acc, want[0]) and np.array_equal(nxt, want[1]) and np.array_equal(com, want[2])

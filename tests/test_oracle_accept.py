@@ -117,7 +117,8 @@ def test_noise_uniform_matches_scalar_definition():
     got = noise_uniform(seed, row, toks)
     for t, g in zip(toks, got):
         z = splitmix64_at(seed, row * (1 << 32) + int(t))
-        assert g == ((z >> 40) + 0.5) / (1 << 24)
+        assert g == ((z >> 41) + 0.5) / (1 << 23)
+        assert np.float32(g) == g                      # exact in float32
     assert np.all((got > 0) & (got < 1))
 
 
