@@ -62,6 +62,10 @@ __device__ __forceinline__ void place_code(int e, uint32_t c, uint32_t (&w)[3]) 
 
 template <typename T>
 __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
+    // launched with programmatic stream serialisation: let the next grid be
+    // scheduled, and wait for the previous one before reading anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int slot = blockIdx.y;
     const int t = blockIdx.x;
     const int n_new = a.n_new[slot];
@@ -169,10 +173,17 @@ __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
     if (a.max_n_new == 0 || a.num_slots == 0) return cudaSuccess;
-    dim3 grid((unsigned)a.max_n_new, (unsigned)a.num_slots);
-    if (a.dtype == Q3KV_F32) append_kernel<float><<<grid, 128, 0, stream>>>(a);
-    else append_kernel<__nv_bfloat16><<<grid, 128, 0, stream>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.max_n_new, (unsigned)a.num_slots);
+    cfg.blockDim = dim3(128);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (a.dtype == Q3KV_F32) return cudaLaunchKernelEx(&cfg, append_kernel<float>, a);
+    return cudaLaunchKernelEx(&cfg, append_kernel<__nv_bfloat16>, a);
 }
 
 }  // namespace q3kv

@@ -50,7 +50,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(VerifyArgs a, int 
     const int g = (unit / a.row_chunks) % a.num_kv_heads;
     const int slot = unit / (a.row_chunks * a.num_kv_heads);
 
-    // the verify kernel's partials (and the lengths it validated) are complete
+    // the next grid may be scheduled now; the verify kernel's partials (and
+    // the lengths it validated) are complete after the wait
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const int T = a.n_q[slot];

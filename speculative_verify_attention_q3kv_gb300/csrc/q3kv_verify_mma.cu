@@ -496,7 +496,10 @@ __device__ __forceinline__ __half scale_of(const uint32_t (&sc)[4], int b) {
 // hi/lo split.
 template <typename TIn>
 __global__ void __launch_bounds__(256) qprep_kernel(VerifyArgs a) {
-    // the verify grid may start now; it waits for this grid before reading Q
+    // wait for the previous grid before reading anything; only then let the
+    // verify grid start (it reads the cache and lengths before its own wait,
+    // which covers only the queries written here)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int unit = blockIdx.x;
@@ -824,22 +827,21 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         if (ok) {
             const int unit = (slot * a.num_kv_heads + g) * a.row_chunks + chunk;
             float* po = a.part_o + ((int64_t)unit * a.num_splits + split) * kRows * kHeadDim;
+            // one TMEM round trip per O^T half (all its columns loaded, then stored)
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
                 const int d = 128 * h + 32 * q + lane;
                 const uint32_t col = h ? kColO1 : kColO0;
-#pragma unroll 1
-                for (int c = 0; c < N; c += 16) {
-                    float v16[16];
-                    tmem_ld16(tmem + lane_base + col + c, v16);
-                    tmem_ld_wait();
+                float v[kRows];
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const int r = c + k;
-                        if (r < Rc) {
-                            if (n_splits == 1) outs[r * kHeadDim + d] = v16[k] / sm.l_run[r];
-                            else po[r * kHeadDim + d] = v16[k];
-                        }
+                for (int c = 0; c < 4; ++c)
+                    if (16 * c < N) tmem_ld16(tmem + lane_base + col + 16 * c, &v[16 * c]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) {
+                    if (r < Rc) {
+                        if (n_splits == 1) outs[r * kHeadDim + d] = v[r] / sm.l_run[r];
+                        else po[r * kHeadDim + d] = v[r];
                     }
                 }
             }
@@ -1086,9 +1088,19 @@ cudaError_t launch_typed(const VerifyArgs& a, cudaStream_t stream, bool& attr_se
         attr_set = true;
     }
     const unsigned units = (unsigned)(a.num_slots * a.num_kv_heads * a.row_chunks);
-    qprep_kernel<TIn><<<dim3(units, kRows / 8), 256, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    {
+        cudaLaunchConfig_t qc = {};
+        qc.gridDim = dim3(units, kRows / 8);
+        qc.blockDim = dim3(256);
+        qc.stream = stream;
+        qc.attrs = attr;
+        qc.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&qc, qprep_kernel<TIn>, a);
+        if (e != cudaSuccess) return e;
+    }
     // the verify grid may start while the query kernel runs: only its QK
     // issuer waits (griddepcontrol.wait) for the queries
     cudaLaunchConfig_t cfg = {};
@@ -1096,9 +1108,6 @@ cudaError_t launch_typed(const VerifyArgs& a, cudaStream_t stream, bool& attr_se
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, verify_mma_kernel<TIn>, a);
