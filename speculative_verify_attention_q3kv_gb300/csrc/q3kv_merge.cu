@@ -35,8 +35,9 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// e^x (natural units) or 2^x (log2 units); -inf gives 0
 template <bool LOG2>
-__device__ __forceinline__ float pexp(float x) { return LOG2 ? exp2f(x) : expf(x); }
+__device__ __forceinline__ float pexp(float x) { return LOG2 ? exp2f(x) : __expf(x); }
 
 template <bool LOG2>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(VerifyArgs a, int rows_per_chunk) {
@@ -82,19 +83,19 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(VerifyArgs a, int 
     }
 
     // ---- M, the denominator and the weights from one read of the (m, l)
-    // pairs (held in registers when there are at most 2048 splits)
+    // pairs (held in registers for the first 2048 splits; any further ones are
+    // read again in each pass)
     constexpr int kPerThread = kWChunk / kMergeThreads;
-    const bool in_regs = n_splits <= kWChunk;
     float2 ml[kPerThread];
     float M = -CUDART_INF_F;
-    for (int i0 = 0; i0 < n_splits; i0 += kWChunk) {
 #pragma unroll
-        for (int k = 0; k < kPerThread; ++k) {
-            const int i = i0 + k * kMergeThreads + tid;
-            ml[k] = i < n_splits ? __ldcg(pml + i * ml_stride) : make_float2(-CUDART_INF_F, 0.0f);
-            M = fmaxf(M, ml[k].x);
-        }
+    for (int k = 0; k < kPerThread; ++k) {
+        const int i = k * kMergeThreads + tid;
+        ml[k] = i < n_splits ? __ldcg(pml + i * ml_stride) : make_float2(-CUDART_INF_F, 0.0f);
+        M = fmaxf(M, ml[k].x);
     }
+#pragma unroll 1
+    for (int i = kWChunk + tid; i < n_splits; i += kMergeThreads) M = fmaxf(M, __ldcg(pml + i * ml_stride).x);
     M = warp_max(M);
     if (lane == 0) red[0][warp] = M;
     __syncthreads();
@@ -102,20 +103,15 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(VerifyArgs a, int 
 #pragma unroll
     for (int k = 1; k < kMergeThreads / 32; ++k) M = fmaxf(M, red[0][k]);
     float den = 0.0f;
-    if (in_regs) {
 #pragma unroll
-        for (int k = 0; k < kPerThread; ++k)
-            if (ml[k].x != -CUDART_INF_F) {
-                ml[k].x = pexp<LOG2>(ml[k].x - M);   // e^(m_i - M)
-                den += ml[k].x * ml[k].y;
-            } else {
-                ml[k].x = 0.0f;
-            }
-    } else {
-        for (int i = tid; i < n_splits; i += kMergeThreads) {
-            const float2 v = __ldcg(pml + i * ml_stride);
-            if (v.x != -CUDART_INF_F) den += pexp<LOG2>(v.x - M) * v.y;
-        }
+    for (int k = 0; k < kPerThread; ++k) {
+        ml[k].x = pexp<LOG2>(ml[k].x - M);           // e^(m_i - M); 0 for the padding
+        den = fmaf(ml[k].x, ml[k].y, den);
+    }
+#pragma unroll 1
+    for (int i = kWChunk + tid; i < n_splits; i += kMergeThreads) {
+        const float2 v = __ldcg(pml + i * ml_stride);
+        den = fmaf(pexp<LOG2>(v.x - M), v.y, den);
     }
     den = warp_sum(den);
     if (lane == 0) red[1][warp] = den;
@@ -125,35 +121,31 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(VerifyArgs a, int 
     for (int k = 0; k < kMergeThreads / 32; ++k) den += red[1][k];
     const float inv = 1.0f / den;
 
-    // ---- o = sum_i w_i o_i
+    // ---- o = sum_i w_i o_i, in passes of 2048 splits
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 1
     for (int i0 = 0; i0 < n_splits; i0 += kWChunk) {
         const int ni = min(kWChunk, n_splits - i0);
-        if (in_regs) {
+        if (i0 == 0) {
 #pragma unroll
-            for (int k = 0; k < kPerThread; ++k) {
-                const int i = k * kMergeThreads + tid;
-                if (i < ni) w[i] = ml[k].x * inv;
-            }
+            for (int k = 0; k < kPerThread; ++k) w[k * kMergeThreads + tid] = ml[k].x * inv;
         } else {
-            for (int i = tid; i < ni; i += kMergeThreads) {
-                const float2 v = __ldcg(pml + (i0 + i) * ml_stride);
-                w[i] = (v.x == -CUDART_INF_F) ? 0.0f : pexp<LOG2>(v.x - M) * inv;
-            }
+#pragma unroll 1
+            for (int i = tid; i < ni; i += kMergeThreads) w[i] = pexp<LOG2>(__ldcg(pml + (i0 + i) * ml_stride).x - M) * inv;
         }
         __syncthreads();
         int i = sg;
         if (i0 == 0) {
 #pragma unroll
             for (int k = 0; k < kOPre; ++k, i += 4) {
-                const float wi = i < ni ? w[i] : 0.0f;
+                const float wi = w[i];                   // 0 past the last split (padding weights)
                 acc.x = fmaf(wi, ov[k].x, acc.x);
                 acc.y = fmaf(wi, ov[k].y, acc.y);
                 acc.z = fmaf(wi, ov[k].z, acc.z);
                 acc.w = fmaf(wi, ov[k].w, acc.w);
             }
         }
-#pragma unroll 8
+#pragma unroll 1
         for (; i < ni; i += 4) {
             const float4 v = __ldcg(reinterpret_cast<const float4*>(po4 + (i0 + i) * o_stride));
             const float wi = w[i];

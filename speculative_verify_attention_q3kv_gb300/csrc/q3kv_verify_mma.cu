@@ -445,26 +445,6 @@ __device__ __forceinline__ int32_t tile_page(const VerifyArgs& a, const int32_t*
     return (page >= 0 && page < a.num_pages) ? page : -1;
 }
 
-// One 112-byte record from a shared-memory stage (7 x 16-byte loads; lanes
-// 112 bytes apart hit eight distinct 16-byte bank groups), or zeros.
-__device__ __forceinline__ void load_record(const uint8_t* rec, bool valid, uint32_t (&w)[24], uint32_t (&sc)[4]) {
-    if (valid) {
-        const uint4* p = reinterpret_cast<const uint4*>(rec);
-#pragma unroll
-        for (int k = 0; k < 6; ++k) {
-            const uint4 u = p[k];
-            w[4 * k] = u.x; w[4 * k + 1] = u.y; w[4 * k + 2] = u.z; w[4 * k + 3] = u.w;
-        }
-        const uint4 s = p[6];
-        sc[0] = s.x; sc[1] = s.y; sc[2] = s.z; sc[3] = s.w;
-    } else {
-#pragma unroll
-        for (int k = 0; k < 24; ++k) w[k] = 0u;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) sc[k] = 0u;
-    }
-}
-
 // Issues the bulk copy of n records (kv 0 = K, 1 = V) of the tile at pos0,
 // starting at row r0 of the tile, or, for a page id out of range, flags it
 // and completes the phase without data (the readers zero that tile).
@@ -482,11 +462,6 @@ __device__ __forceinline__ void issue_rec_copy(const VerifyArgs& a, const int32_
     fence_proxy_async();
     mbar_arrive_expect_tx(full, bytes);
     bulk_g2s(dst, src, bytes, full);
-}
-
-__device__ __forceinline__ __half scale_of(const uint32_t (&sc)[4], int b) {
-    const uint32_t u = sc[b >> 1];
-    return __ushort_as_half((unsigned short)((b & 1) ? (u >> 16) : (u & 0xFFFFu)));
 }
 
 // Rotated queries of one unit (slot, kv head, 64-row chunk) in the verify
@@ -818,7 +793,11 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
             sm.red[q][lane] = transpose_reduce<false>(*reinterpret_cast<float(*)[32]>(&y[0]));
             if (N > 32) sm.red[q][32 + lane] = transpose_reduce<false>(*reinterpret_cast<float(*)[32]>(&y[32]));
             named_sync(kBarA, 128);
-            if (tid < N) sm.l_run[tid] = (sm.red[0][tid] + sm.red[1][tid]) + (sm.red[2][tid] + sm.red[3][tid]);
+            if (tid < N) {
+                const float l = (sm.red[0][tid] + sm.red[1][tid]) + (sm.red[2][tid] + sm.red[3][tid]);
+                sm.l_run[tid] = l;
+                sm.alpha[tid] = (n_splits == 1) ? 1.0f / l : 1.0f;   // the epilogue's row multiplier
+            }
         }
         named_sync(kBarA, 128);   // l_run complete
         // ---- epilogue: O^T -> partial or finished rows
@@ -827,22 +806,21 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         if (ok) {
             const int unit = (slot * a.num_kv_heads + g) * a.row_chunks + chunk;
             float* po = a.part_o + ((int64_t)unit * a.num_splits + split) * kRows * kHeadDim;
-            // one TMEM round trip per O^T half (all its columns loaded, then stored)
+            // 16 rows of this thread's dim per TMEM round trip: a short loop,
+            // since this code runs once per CTA and is fetched cold
+            float* dst = (n_splits == 1) ? outs : po;
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
                 const int d = 128 * h + 32 * q + lane;
                 const uint32_t col = h ? kColO1 : kColO0;
-                float v[kRows];
+#pragma unroll 1
+                for (int c = 0; c < Rc; c += 16) {
+                    float v[16];
+                    tmem_ld16(tmem + lane_base + col + c, v);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    if (16 * c < N) tmem_ld16(tmem + lane_base + col + 16 * c, &v[16 * c]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int r = 0; r < kRows; ++r) {
-                    if (r < Rc) {
-                        if (n_splits == 1) outs[r * kHeadDim + d] = v[r] / sm.l_run[r];
-                        else po[r * kHeadDim + d] = v[r];
-                    }
+                    for (int k = 0; k < 16; ++k)
+                        if (c + k < Rc) dst[(c + k) * kHeadDim + d] = v[k] * sm.alpha[c + k];
                 }
             }
             if (n_splits > 1 && tid < Rc) {
