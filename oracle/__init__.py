@@ -9,7 +9,9 @@ A plain, slow, obviously correct restatement of what the hot path computes:
                    exactly dequantised values, GQA group by group;
 * ``cache``     -- an oracle-side paged cache: append and read back;
 * ``accept``    -- greedy acceptance of a verify step's drafts and the commit
-                   (rollback) of the cache length.
+                   (rollback) of the cache length;
+* ``fp8``       -- the fp8 E4M3 comparison format (saturating, unscaled,
+                   unrotated), its paged cache and plain-basis attention.
 
 Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
 may import this package.  The product path (the CUDA library and its Python
