@@ -10,8 +10,9 @@ step / device time of a step) with the cache and the step's inputs resident on
 the device; ``e2e`` = the same metric through the same C-ABI calls with the
 step's inputs copied from pinned host memory and the outputs copied back inside
 the timed region.  ``roofline`` describes the verify kernel: algorithmic KV
-bytes per launch (224 bytes per attended position per kv head) over its mean
-CUDA-event duration.  ``--impl reference`` times the CPU oracle instead.
+bytes per launch (224 bytes per attended position per kv head; 512 with
+``--kv fp8``, the fp8 E4M3 comparison cache) over its mean CUDA-event duration.
+``--impl reference`` times the CPU oracle instead.
 
 Multi-GPU: replicas only (one independent replica per rank, no collective on
 the data path); ``value`` sums all ranks' tokens over the slowest rank's time.
@@ -54,6 +55,8 @@ def parse():
     ap.add_argument("--split", type=int, default=0, help="positions per split (0 = library policy)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv", default="q3", choices=["q3", "fp8"],
+                    help="cache format: the 3-bit rotated codec, or the fp8 E4M3 comparison format")
     return ap.parse_args()
 
 
@@ -157,7 +160,7 @@ def measured_peak_hbm():
 class Step:
     """Device buffers and the per-layer append + verify calls of one workload step."""
 
-    def __init__(self, w, verify_impl, split, device):
+    def __init__(self, w, verify_impl, split, device, kv="q3"):
         import torch
 
         from speculative_verify_attention_q3kv_gb300 import api
@@ -173,7 +176,12 @@ class Step:
         pages = [(n + 255) // 256 for n in self.Ltot]
         self.num_pages = sum(pages)
         self.desc = api.make_desc(w.num_layers, w.num_kv_heads, self.num_pages)
-        self.pool = torch.zeros(api.pool_bytes(self.desc), dtype=torch.uint8, device=device)
+        self.fp8 = kv == "fp8"
+        self.record_bytes = 256 if self.fp8 else 112
+        self._append = api.fp8_append if self.fp8 else api.append
+        self._verify = api.fp8_verify_attn if self.fp8 else api.verify_attn
+        pool_bytes = api.fp8_pool_bytes(self.desc) if self.fp8 else api.pool_bytes(self.desc)
+        self.pool = torch.zeros(pool_bytes, dtype=torch.uint8, device=device)
         pt = np.full((self.S, max(pages)), -1, np.int32)
         k = 0
         for b, n in enumerate(pages):
@@ -239,24 +247,24 @@ class Step:
                     nn[b] = n
                     offs = torch.zeros(self.S + 1, dtype=torch.int32, device=self.device)
                     offs[b + 1:] = n
-                    api.append(self.desc, self.pool, self.page_table, lens, nn, offs, n, l, kk, vv, self.status)
+                    self._append(self.desc, self.pool, self.page_table, lens, nn, offs, n, l, kk, vv, self.status)
         torch.cuda.synchronize()
         assert int(self.status.item()) == 0, "prefill flagged a device status"
 
     def kv_bytes_per_layer(self):
-        return sum(self.Ltot) * self.w.num_kv_heads * 224
+        return sum(self.Ltot) * self.w.num_kv_heads * 2 * self.record_bytes
 
     def run(self, append=True, verify=True):
         """One step: for every layer, append the new K/V then verify the new tokens."""
         api = self.api
         for l in range(self.w.num_layers):
             if append:
-                api.append(self.desc, self.pool, self.page_table, self.slot_len, self.n_new_d, self.row_off,
-                           self.max_new, l, self.k_new[l], self.v_new[l], self.status)
+                self._append(self.desc, self.pool, self.page_table, self.slot_len, self.n_new_d, self.row_off,
+                             self.max_new, l, self.k_new[l], self.v_new[l], self.status)
             if verify:
-                api.verify_attn(self.desc, self.pool, self.page_table, self.ctx_len, self.n_new_d, self.row_off,
-                                self.max_ctx, self.max_new, l, self.q[l], self.out[l], self.ws, self.impl,
-                                self.split, self.status)
+                self._verify(self.desc, self.pool, self.page_table, self.ctx_len, self.n_new_d, self.row_off,
+                             self.max_ctx, self.max_new, l, self.q[l], self.out[l], self.ws, self.impl,
+                             self.split, self.status)
 
     def accept(self):
         """Greedy acceptance of the step's drafts and the committed lengths (once per step)."""
@@ -299,7 +307,7 @@ def run_ours(args, rank, world, local, pg):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     w = qi.WORKLOADS[args.workload]
-    st = Step(w, args.verify_impl, args.split, device)
+    st = Step(w, args.verify_impl, args.split, device, kv=args.kv)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     tokens_per_step = sum(st.n_new)
     Ly = w.num_layers
@@ -383,7 +391,7 @@ def run_ours(args, rank, world, local, pg):
     kv_bytes = st.kv_bytes_per_layer()
     achieved = kv_bytes / mean_verify_s / 1e9
     cpu = None
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline and world == 1 and args.kv == "q3":
         cpu = cpu_baseline(w, budget_s=20.0)
     line = {
         "metric": METRIC,
@@ -399,7 +407,10 @@ def run_ours(args, rank, world, local, pg):
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded; K,V per-channel 10^U(0,1) outliers, Q N(0,1))" if w.kv_dist == "loguniform10"
                 else "synthetic (seeded; K,V N(0,1) with 4 outlier channels x8)",
-        "config": {"workload": w.name, "slots": w.num_slots, "layers": Ly, "kv_heads": w.num_kv_heads,
+        "config": {"workload": w.name if args.kv == "q3" else w.name + "_fp8kv",
+                   "kv_format": "q3kv 3-bit WHT, 112 B per head vector" if args.kv == "q3"
+                   else "fp8 e4m3, 256 B per head vector",
+                   "slots": w.num_slots, "layers": Ly, "kv_heads": w.num_kv_heads,
                    "q_heads": w.num_q_heads, "head_dim": w.head_dim, "ctx": st.ctx, "query_tokens": st.n_new,
                    "page_size": 256, "verify_impl": args.verify_impl, "split_positions": args.split,
                    "l2": "flushed between timed steps (256 MiB write)", "launch": "CUDA graph per step",
@@ -408,7 +419,7 @@ def run_ours(args, rank, world, local, pg):
         "verify_only_tokens_per_s": tokens_per_step * args.steps / (sum(verify_ms) / 1e3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
-                     "traffic": NCU_TRAFFIC_BYTES.get(w.key) if args.verify_impl == "auto" else None,
+                     "traffic": NCU_TRAFFIC_BYTES.get(w.key) if args.verify_impl == "auto" and args.kv == "q3" else None,
                      "kernel": "q3kv_verify_attn per layer (query + verify + split-merge kernels)",
                      "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": kv_bytes,

@@ -215,6 +215,36 @@ Q3KV_API int q3kv_verify_attn_noalloc(void* stream, const q3kv_cache_desc* desc,
                      const void* q, int32_t dtype, float* out,
                      int32_t impl, int32_t split_positions, int32_t* d_status);
 
+/* ---- fp8 E4M3 comparison cache ------------------------------------------------
+ * The format the pages' server uses by default ("KV cache" stack bullet of the
+ * "Quasar" (q27) wiki): K and V stored as fp8 E4M3 with a scale-free,
+ * saturating conversion and no rotation.  It exists here to measure what the
+ * 3-bit cache buys: 512 bytes per (position, kv head) against 224.
+ *   - Record: 256 E4M3 bytes (dims in order) per head vector; pages, page
+ *     tables, lengths and allocator exactly as the 3-bit cache, with 256-byte
+ *     records in place of 112-byte ones.
+ *   - Conversion: round to nearest (ties to even mantissa); magnitudes above
+ *     448 and infinities to +-448; NaN stays NaN and, like an infinity, sets
+ *     Q3KV_STATUS_NONFINITE_INPUT.
+ *   - Verify: out = softmax(q . k / 16) v over the decoded values (no
+ *     rotation), on the tensor-core leg only (impl AUTO or MMA; FMA returns
+ *     Q3KV_ERR_UNSUPPORTED).  Its workspace is q3kv_workspace_bytes(...) with
+ *     the same arguments.
+ * Arguments, ownership, errors and status bits are those of q3kv_pool_bytes,
+ * q3kv_append and q3kv_verify_attn. */
+Q3KV_API int q3kv_fp8_pool_bytes(const q3kv_cache_desc* desc, size_t* bytes);
+Q3KV_API int q3kv_fp8_append(void* stream, const q3kv_cache_desc* desc, void* d_pool, const int32_t* d_page_table,
+                    int32_t max_pages_per_slot, const int32_t* d_slot_len, const int32_t* d_n_new,
+                    const int32_t* d_row_offsets, int32_t num_slots, int32_t max_n_new, int32_t layer,
+                    const void* k, const void* v, int32_t dtype, int32_t* d_status);
+Q3KV_API int q3kv_fp8_verify_attn(void* stream, const q3kv_cache_desc* desc, const void* d_pool,
+                     const int32_t* d_page_table, int32_t max_pages_per_slot,
+                     const int32_t* d_ctx_len, const int32_t* d_n_q, const int32_t* d_q_offsets,
+                     int32_t num_slots, int64_t max_ctx_len, int32_t max_n_q, int32_t layer,
+                     const void* q, int32_t dtype, float* out,
+                     int32_t impl, int32_t split_positions,
+                     void* d_workspace, size_t workspace_bytes, int32_t* d_status);
+
 /* ---- greedy acceptance and commit ------------------------------------------
  * Source: "Quasar" (q27) wiki -- the sampler paragraph of "Serving" and the
  * "Model tool protocol" bullet (greedy speculative decode is the default), and

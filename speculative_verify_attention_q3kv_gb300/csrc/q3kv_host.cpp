@@ -181,7 +181,11 @@ int q3kv_free_pages(const q3kv_allocator* a, int32_t* n_free) {
     return Q3KV_OK;
 }
 
-int q3kv_append(void* stream, const q3kv_cache_desc* desc, void* d_pool, const int32_t* d_page_table,
+}  // extern "C"
+
+namespace {
+
+int append_impl(int fmt, void* stream, const q3kv_cache_desc* desc, void* d_pool, const int32_t* d_page_table,
                 int32_t max_pages_per_slot, const int32_t* d_slot_len, const int32_t* d_n_new,
                 const int32_t* d_row_offsets, int32_t num_slots, int32_t max_n_new, int32_t layer, const void* k,
                 const void* v, int32_t dtype, int32_t* d_status) {
@@ -211,26 +215,15 @@ int q3kv_append(void* stream, const q3kv_cache_desc* desc, void* d_pool, const i
     a.v = v;
     a.dtype = dtype;
     a.status = d_status;
-    return cuda_status(launch_append(a, static_cast<cudaStream_t>(stream)));
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return cuda_status(fmt == kFmtFp8 ? launch_append_fp8(a, st) : launch_append(a, st));
 }
 
-int q3kv_workspace_bytes(const q3kv_cache_desc* desc, int32_t num_slots, int64_t max_ctx_len, int32_t max_n_q,
-                         int32_t impl, int32_t split_positions, size_t* bytes) {
-    int e = check_desc(desc);
-    if (e != Q3KV_OK) return e;
-    if (!bytes) return Q3KV_ERR_INVALID_ARG;
-    Plan p;
-    e = make_plan(desc, num_slots, max_ctx_len, max_n_q, impl, split_positions, &p);
-    if (e != Q3KV_OK) return e;
-    *bytes = p.total();
-    return Q3KV_OK;
-}
-
-int q3kv_verify_attn(void* stream, const q3kv_cache_desc* desc, const void* d_pool, const int32_t* d_page_table,
-                     int32_t max_pages_per_slot, const int32_t* d_ctx_len, const int32_t* d_n_q,
-                     const int32_t* d_q_offsets, int32_t num_slots, int64_t max_ctx_len, int32_t max_n_q,
-                     int32_t layer, const void* q, int32_t dtype, float* out, int32_t impl,
-                     int32_t split_positions, void* d_workspace, size_t workspace_bytes, int32_t* d_status) {
+int verify_impl(int fmt, void* stream, const q3kv_cache_desc* desc, const void* d_pool, const int32_t* d_page_table,
+                int32_t max_pages_per_slot, const int32_t* d_ctx_len, const int32_t* d_n_q,
+                const int32_t* d_q_offsets, int32_t num_slots, int64_t max_ctx_len, int32_t max_n_q,
+                int32_t layer, const void* q, int32_t dtype, float* out, int32_t impl,
+                int32_t split_positions, void* d_workspace, size_t workspace_bytes, int32_t* d_status) {
     int e = check_desc(desc);
     if (e != Q3KV_OK) return e;
     if (num_slots < 0 || max_pages_per_slot <= 0 || layer < 0 || layer >= desc->num_layers)
@@ -239,6 +232,7 @@ int q3kv_verify_attn(void* stream, const q3kv_cache_desc* desc, const void* d_po
     if (dtype != Q3KV_F32 && dtype != Q3KV_BF16) return Q3KV_ERR_INVALID_ARG;
     if (max_n_q > kMaxNq) return Q3KV_ERR_UNSUPPORTED;
     if (impl < Q3KV_IMPL_AUTO || impl > Q3KV_IMPL_MMA) return Q3KV_ERR_INVALID_ARG;
+    if (fmt == kFmtFp8 && impl == Q3KV_IMPL_FMA) return Q3KV_ERR_UNSUPPORTED;   // tensor-core leg only
     Plan p;
     e = make_plan(desc, num_slots, max_ctx_len, max_n_q, impl, split_positions, &p);
     if (e != Q3KV_OK) return e;
@@ -275,12 +269,73 @@ int q3kv_verify_attn(void* stream, const q3kv_cache_desc* desc, const void* d_po
     a.part_o = p.part_o_bytes ? reinterpret_cast<float*>(ws) : nullptr;
     a.part_ml = p.part_ml_bytes ? reinterpret_cast<float*>(ws + p.part_o_bytes) : nullptr;
     a.q_prep = p.q_prep_bytes ? static_cast<void*>(ws + p.part_o_bytes + p.part_ml_bytes) : nullptr;
+    a.fmt = fmt;
     a.status = d_status;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool mma = (p.impl == Q3KV_IMPL_MMA);
     cudaError_t ce = mma ? launch_verify_mma(a, st) : launch_verify_fma(a, st);
     if (ce == cudaSuccess) ce = launch_merge(a, p.rows_per_chunk, mma, st);
     return cuda_status(ce);
+}
+
+}  // namespace
+
+extern "C" {
+
+int q3kv_append(void* stream, const q3kv_cache_desc* desc, void* d_pool, const int32_t* d_page_table,
+                int32_t max_pages_per_slot, const int32_t* d_slot_len, const int32_t* d_n_new,
+                const int32_t* d_row_offsets, int32_t num_slots, int32_t max_n_new, int32_t layer, const void* k,
+                const void* v, int32_t dtype, int32_t* d_status) {
+    return append_impl(kFmtQ3, stream, desc, d_pool, d_page_table, max_pages_per_slot, d_slot_len, d_n_new,
+                       d_row_offsets, num_slots, max_n_new, layer, k, v, dtype, d_status);
+}
+
+int q3kv_verify_attn(void* stream, const q3kv_cache_desc* desc, const void* d_pool, const int32_t* d_page_table,
+                     int32_t max_pages_per_slot, const int32_t* d_ctx_len, const int32_t* d_n_q,
+                     const int32_t* d_q_offsets, int32_t num_slots, int64_t max_ctx_len, int32_t max_n_q,
+                     int32_t layer, const void* q, int32_t dtype, float* out, int32_t impl,
+                     int32_t split_positions, void* d_workspace, size_t workspace_bytes, int32_t* d_status) {
+    return verify_impl(kFmtQ3, stream, desc, d_pool, d_page_table, max_pages_per_slot, d_ctx_len, d_n_q,
+                       d_q_offsets, num_slots, max_ctx_len, max_n_q, layer, q, dtype, out, impl, split_positions,
+                       d_workspace, workspace_bytes, d_status);
+}
+
+int q3kv_workspace_bytes(const q3kv_cache_desc* desc, int32_t num_slots, int64_t max_ctx_len, int32_t max_n_q,
+                         int32_t impl, int32_t split_positions, size_t* bytes) {
+    int e = check_desc(desc);
+    if (e != Q3KV_OK) return e;
+    if (!bytes) return Q3KV_ERR_INVALID_ARG;
+    Plan p;
+    e = make_plan(desc, num_slots, max_ctx_len, max_n_q, impl, split_positions, &p);
+    if (e != Q3KV_OK) return e;
+    *bytes = p.total();
+    return Q3KV_OK;
+}
+
+int q3kv_fp8_pool_bytes(const q3kv_cache_desc* desc, size_t* bytes) {
+    int e = check_desc(desc);
+    if (e != Q3KV_OK) return e;
+    if (!bytes) return Q3KV_ERR_INVALID_ARG;
+    *bytes = (size_t)desc->num_pages * desc->num_layers * desc->num_kv_heads * 2 * kPageSize * kFp8RecordBytes;
+    return Q3KV_OK;
+}
+
+int q3kv_fp8_append(void* stream, const q3kv_cache_desc* desc, void* d_pool, const int32_t* d_page_table,
+                    int32_t max_pages_per_slot, const int32_t* d_slot_len, const int32_t* d_n_new,
+                    const int32_t* d_row_offsets, int32_t num_slots, int32_t max_n_new, int32_t layer,
+                    const void* k, const void* v, int32_t dtype, int32_t* d_status) {
+    return append_impl(kFmtFp8, stream, desc, d_pool, d_page_table, max_pages_per_slot, d_slot_len, d_n_new,
+                       d_row_offsets, num_slots, max_n_new, layer, k, v, dtype, d_status);
+}
+
+int q3kv_fp8_verify_attn(void* stream, const q3kv_cache_desc* desc, const void* d_pool,
+                         const int32_t* d_page_table, int32_t max_pages_per_slot, const int32_t* d_ctx_len,
+                         const int32_t* d_n_q, const int32_t* d_q_offsets, int32_t num_slots, int64_t max_ctx_len,
+                         int32_t max_n_q, int32_t layer, const void* q, int32_t dtype, float* out, int32_t impl,
+                         int32_t split_positions, void* d_workspace, size_t workspace_bytes, int32_t* d_status) {
+    return verify_impl(kFmtFp8, stream, desc, d_pool, d_page_table, max_pages_per_slot, d_ctx_len, d_n_q,
+                       d_q_offsets, num_slots, max_ctx_len, max_n_q, layer, q, dtype, out, impl, split_positions,
+                       d_workspace, workspace_bytes, d_status);
 }
 
 }  // extern "C"

@@ -17,11 +17,19 @@ constexpr int kCodeWords = 24;       // 96 bytes of codes
 constexpr int kMaxNq = 16;           // query tokens per slot and step
 constexpr int kMaxRows = kGroup * kMaxNq;
 
-// Byte offset of a record inside the pool (see q3kv_pool_bytes).
+constexpr int kFp8RecordBytes = 256;  // fp8 E4M3 comparison format: one byte per element
+
+// Cache formats: the 3-bit rotated codec, and the fp8 E4M3 comparison format.
+constexpr int kFmtQ3 = 0;
+constexpr int kFmtFp8 = 1;
+
+// Byte offset of a record inside the pool (see q3kv_pool_bytes); records of
+// rec_bytes bytes (112 for the 3-bit codec, 256 for fp8).
 __host__ __device__ inline size_t record_offset(int num_layers, int num_kv_heads, int64_t page,
-                                                int layer, int kv_head, int kv, int row) {
+                                                int layer, int kv_head, int kv, int row,
+                                                int rec_bytes = kRecordBytes) {
     return (size_t)((((page * num_layers + layer) * num_kv_heads + kv_head) * 2 + kv) * kPageSize + row) *
-           kRecordBytes;
+           rec_bytes;
 }
 
 // Everything a verify launch needs, resolved on the host.
@@ -46,7 +54,8 @@ struct VerifyArgs {
     int32_t row_chunks;        // CTAs along the query rows of one kv head
     float* part_o;             // [slots, kv_heads, row_chunks, splits, rows_per_chunk, 256]
     float* part_ml;            // [slots, kv_heads, row_chunks, splits, rows_per_chunk, 2]
-    void* q_prep;              // tensor-core leg: [unit][hi|lo][64 x 256] fp16 rotated queries
+    void* q_prep;              // tensor-core leg: [unit][hi|lo][64 x 256] fp16 (rotated) queries
+    int32_t fmt;               // kFmtQ3 or kFmtFp8
     int32_t* status;
 };
 
@@ -101,6 +110,7 @@ cudaError_t launch_accept_sample(const AcceptArgs& a, cudaStream_t stream);
 // FMA (CUDA-core) leg: rows per CTA, and its workspace/launch.
 constexpr int kFmaRows = 64;
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
+cudaError_t launch_append_fp8(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_verify_fma(const VerifyArgs& a, cudaStream_t stream);
 // tcgen05 leg: 64 rows per CTA, one CTA per SM (shared memory bound); the
 // rotated fp16 hi/lo queries of one unit, as the kernel's B operand of QK.

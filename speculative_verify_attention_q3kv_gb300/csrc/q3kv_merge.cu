@@ -4,7 +4,8 @@
 // For a row with partials (m_i, l_i, o_i) from splits i:
 //   M = max_i m_i,  w_i = e^(m_i - M) / sum_j e^(m_j - M) l_j,  o = sum_i w_i o_i
 // (base-2 exponentials for the tensor-core leg, whose scores are in log2
-// units), then out = H o / 16 back in the unrotated basis.
+// units), then out = H o / 16 back in the unrotated basis (the fp8 cache is
+// not rotated: out = o).
 //
 // The kernel is launched with programmatic stream serialisation: its CTAs may
 // start while the verify kernel finishes and wait (griddepcontrol.wait) for
@@ -39,7 +40,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 template <bool LOG2>
 __device__ __forceinline__ float pexp(float x) { return LOG2 ? exp2f(x) : __expf(x); }
 
-template <bool LOG2>
+template <bool LOG2, bool ROT>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(VerifyArgs a, int rows_per_chunk) {
     __shared__ float w[kWChunk];
     __shared__ __align__(16) float4 part[4][64];
@@ -160,7 +161,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(VerifyArgs a, int 
     __syncthreads();
     if (warp != 0) return;
 
-    // ---- one warp: sum the split groups, out = H o / 16 (lane holds dims 8 lane .. 8 lane + 7)
+    // ---- one warp: sum the split groups, out = H o / 16 (lane holds dims 8 lane .. 8 lane + 7);
+    // without ROT (the fp8 cache, unrotated) out = o
     float x[8];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -172,32 +174,35 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(VerifyArgs a, int 
         }
         x[4 * h] = t.x; x[4 * h + 1] = t.y; x[4 * h + 2] = t.z; x[4 * h + 3] = t.w;
     }
+    if (ROT) {
 #pragma unroll
-    for (int h = 1; h < 8; h <<= 1)
+        for (int h = 1; h < 8; h <<= 1)
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if ((i & h) == 0) {
-                const float lo = x[i], hi = x[i + h];
-                x[i] = lo + hi;
-                x[i + h] = lo - hi;
+            for (int i = 0; i < 8; ++i)
+                if ((i & h) == 0) {
+                    const float lo = x[i], hi = x[i + h];
+                    x[i] = lo + hi;
+                    x[i + h] = lo - hi;
+                }
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
+                x[i] = upper ? o - x[i] : x[i] + o;
             }
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-        const bool upper = (lane & m) != 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
-            x[i] = upper ? o - x[i] : x[i] + o;
         }
     }
     const int ra = row0 + r;
     const int Hq = a.num_kv_heads * kGroup;
     float* dst = a.out + (((int64_t)a.q_offsets[slot] + ra / kGroup) * Hq + g * kGroup + ra % kGroup) * kHeadDim + 8 * lane;
-    reinterpret_cast<float4*>(dst)[0] = make_float4(x[0] * 0.0625f, x[1] * 0.0625f, x[2] * 0.0625f, x[3] * 0.0625f);
-    reinterpret_cast<float4*>(dst)[1] = make_float4(x[4] * 0.0625f, x[5] * 0.0625f, x[6] * 0.0625f, x[7] * 0.0625f);
+    constexpr float kS = ROT ? 0.0625f : 1.0f;
+    reinterpret_cast<float4*>(dst)[0] = make_float4(x[0] * kS, x[1] * kS, x[2] * kS, x[3] * kS);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(x[4] * kS, x[5] * kS, x[6] * kS, x[7] * kS);
 }
 
-template <bool LOG2>
+template <bool LOG2, bool ROT>
 cudaError_t launch(const VerifyArgs& a, int rows_per_chunk, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)rows_per_chunk, (unsigned)(a.num_slots * a.num_kv_heads * a.row_chunks));
@@ -209,14 +214,15 @@ cudaError_t launch(const VerifyArgs& a, int rows_per_chunk, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, merge_kernel<LOG2>, a, rows_per_chunk);
+    return cudaLaunchKernelEx(&cfg, merge_kernel<LOG2, ROT>, a, rows_per_chunk);
 }
 
 }  // namespace
 
 cudaError_t launch_merge(const VerifyArgs& a, int rows_per_chunk, bool log2_units, cudaStream_t stream) {
     if (a.num_splits <= 1) return cudaSuccess;
-    return log2_units ? launch<true>(a, rows_per_chunk, stream) : launch<false>(a, rows_per_chunk, stream);
+    if (a.fmt == kFmtFp8) return launch<true, false>(a, rows_per_chunk, stream);   // tensor-core leg only
+    return log2_units ? launch<true, true>(a, rows_per_chunk, stream) : launch<false, true>(a, rows_per_chunk, stream);
 }
 
 }  // namespace q3kv

@@ -86,7 +86,21 @@ constexpr int kTileP = 128;                 // positions per tile (MMA M of S^T)
 constexpr int kSubP = 16;                   // positions per V sub-tile (one MMA K step)
 constexpr int kSubTiles = kTileP / kSubP;   // 8
 constexpr int kVBufs = 5;                   // V_hat sub-tile ring (5/8 of a tile)
-constexpr uint32_t kRecTile = kTileP * kRecordBytes;   // 14,336 bytes of records per tile
+// Per cache format: record bytes, whether K_hat / V_hat carry an fp16 lo part
+// (the 3-bit codec's values need 14 significant bits; E4M3 values are exact in
+// fp16), and whether queries and outputs are rotated by H.
+template <int FMT>
+struct Fmt {
+    static constexpr int kRecB = kRecordBytes;
+    static constexpr bool kLo = true;
+    static constexpr bool kRot = true;
+};
+template <>
+struct Fmt<kFmtFp8> {
+    static constexpr int kRecB = kFp8RecordBytes;
+    static constexpr bool kLo = false;
+    static constexpr bool kRot = false;
+};
 constexpr int kRows = 64;                   // max query rows per CTA (MMA N <= 64)
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P <= 256
 // Initial running maximum: finite, so 2^(s - m) of a masked score (-inf) is 0
@@ -123,13 +137,14 @@ struct Bars {
     unsigned long long drain[4];    // everything an issuer started is done (1 commit)
 };
 
+template <int FMT>
 struct __align__(16) MmaSmem {
     __half qhi[kRows * kHeadDim];           // B of QK, K-major core layout
     __half qlo[kRows * kHeadDim];
-    __half v[kVBufs][2][kSubP * kHeadDim];  // [buffer][hi|lo]: A of PV, MN-major
+    __half v[kVBufs][Fmt<FMT>::kLo ? 2 : 1][kSubP * kHeadDim];  // [buffer][hi|lo]: A of PV, MN-major
     __half phi[2][kTileP * kRows];          // B of PV, MN-major, double-buffered by tile
     __half plo[2][kTileP * kRows];
-    uint8_t vrec[kRecTile];                 // V record stage: one 16-record copy per sub-tile
+    uint8_t vrec[kTileP * Fmt<FMT>::kRecB];  // V record stage: one 16-record copy per sub-tile
     float m_run[kRows];
     float thr[kRows];                       // m_run + threshold
     float l_run[kRows];
@@ -367,6 +382,17 @@ __device__ __forceinline__ uint32_t code_pair_last(uint32_t w0, uint32_t w1, uin
 __device__ __forceinline__ __half2 as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 __device__ __forceinline__ uint32_t as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
+// Four E4M3 bytes (b0 lowest) -> fp16 pairs (b0, b1) and (b2, b3), low half
+// first; every E4M3 value is exact in fp16.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& p01, uint32_t& p23) {
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(p01), "=r"(p23)
+        : "r"(w));
+}
+
 // One 32-element block: 16 pairs of (c - 3.5) s_hi and (c - 3.5) s_lo, where
 // s_hi keeps the top 6 significant bits of s and s_lo = s - s_hi the other 5.
 // With x = 8 + c, (c - 3.5) s_part = x s_part - 11.5 s_part: the constant
@@ -448,6 +474,7 @@ __device__ __forceinline__ int32_t tile_page(const VerifyArgs& a, const int32_t*
 // Issues the bulk copy of n records (kv 0 = K, 1 = V) of the tile at pos0,
 // starting at row r0 of the tile, or, for a page id out of range, flags it
 // and completes the phase without data (the readers zero that tile).
+template <int RECB>
 __device__ __forceinline__ void issue_rec_copy(const VerifyArgs& a, const int32_t* pt_row, int g, int kv, int pos0,
                                                int r0, int n, uint8_t* dst, unsigned long long* full) {
     const int32_t page = pt_row[pos0 / kPageSize];
@@ -457,19 +484,20 @@ __device__ __forceinline__ void issue_rec_copy(const VerifyArgs& a, const int32_
         return;
     }
     const uint8_t* src =
-        a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, kv, pos0 % kPageSize + r0);
-    const uint32_t bytes = (uint32_t)(n * kRecordBytes);
+        a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, kv, pos0 % kPageSize + r0, RECB);
+    const uint32_t bytes = (uint32_t)(n * RECB);
     fence_proxy_async();
     mbar_arrive_expect_tx(full, bytes);
     bulk_g2s(dst, src, bytes, full);
 }
 
-// Rotated queries of one unit (slot, kv head, 64-row chunk) in the verify
-// kernel's shared-memory operand layout, fp16 hi then lo; padding rows are
-// zeros.  CTA (unit, group of 8 rows), one row per warp: register butterflies
-// for H, then scale 1/16 (H) * 1/16 (softmax) * log2(e) and a round-to-nearest
+// Queries of one unit (slot, kv head, 64-row chunk) in the verify kernel's
+// shared-memory operand layout, fp16 hi then lo; padding rows are zeros.  CTA
+// (unit, group of 8 rows), one row per warp.  ROT (the 3-bit cache): register
+// butterflies for H, then scale 1/16 (H) * 1/16 (softmax) * log2(e); without
+// ROT (the fp8 cache) only 1/16 (softmax) * log2(e).  Then a round-to-nearest
 // hi/lo split.
-template <typename TIn>
+template <typename TIn, bool ROT>
 __global__ void __launch_bounds__(256) qprep_kernel(VerifyArgs a) {
     // wait for the previous grid before reading anything; only then let the
     // verify grid start (it reads the cache and lengths before its own wait,
@@ -498,29 +526,32 @@ __global__ void __launch_bounds__(256) qprep_kernel(VerifyArgs a) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) y[i] = 0.0f;
     }
+    if (ROT) {
 #pragma unroll
-    for (int h = 1; h < 8; h <<= 1)
+        for (int h = 1; h < 8; h <<= 1)
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if ((i & h) == 0) {
-                const float lo = y[i], hi = y[i + h];
-                y[i] = lo + hi;
-                y[i + h] = lo - hi;
+            for (int i = 0; i < 8; ++i)
+                if ((i & h) == 0) {
+                    const float lo = y[i], hi = y[i + h];
+                    y[i] = lo + hi;
+                    y[i + h] = lo - hi;
+                }
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const float sgn = (lane & m) ? -1.0f : 1.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float o = __shfl_xor_sync(0xffffffffu, y[i], m);
+                y[i] = fmaf(sgn, y[i], o);                    // lower lane: o + y, upper lane: o - y
             }
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-        const float sgn = (lane & m) ? -1.0f : 1.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float o = __shfl_xor_sync(0xffffffffu, y[i], m);
-            y[i] = fmaf(sgn, y[i], o);                    // lower lane: o + y, upper lane: o - y
         }
     }
     uint32_t hw[4], lw[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float x0 = y[2 * i] * (1.4426950408889634f / 256.0f);
-        const float x1 = y[2 * i + 1] * (1.4426950408889634f / 256.0f);
+        constexpr float kScale = ROT ? 1.4426950408889634f / 256.0f : 1.4426950408889634f / 16.0f;
+        const float x0 = y[2 * i] * kScale;
+        const float x1 = y[2 * i + 1] * kScale;
         const __half2 h2 = __floats2half2_rn(x0, x1);
         const float2 hf = __half22float2(h2);
         hw[i] = as_u32(h2);
@@ -530,10 +561,11 @@ __global__ void __launch_bounds__(256) qprep_kernel(VerifyArgs a) {
     *reinterpret_cast<uint4*>(&qlo[q_off(r, 8 * lane)]) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
 }
 
-template <typename TIn>
+template <typename TIn, int FMT>
 __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    MmaSmem& sm = *reinterpret_cast<MmaSmem*>(smem_raw);
+    MmaSmem<FMT>& sm = *reinterpret_cast<MmaSmem<FMT>*>(smem_raw);
+    constexpr int kRecB = Fmt<FMT>::kRecB;
     // the split-merge kernel may be scheduled once every CTA of this grid runs;
     // it waits for this grid's completion before reading the partials
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -615,7 +647,7 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         const int q = warp & 3;
         for (int e = 0; e < 2; ++e) {
             const int r0 = kSubP * (q + 4 * e);
-            issue_rec_copy(a, pt_row, g, 1, p_begin, r0, kSubP, sm.vrec + kRecordBytes * r0, &bar.vfull[q][e]);
+            issue_rec_copy<kRecB>(a, pt_row, g, 1, p_begin, r0, kSubP, sm.vrec + kRecB * r0, &bar.vfull[q][e]);
         }
     }
     if (warp == 12 && lane == 0) {
@@ -834,62 +866,110 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         const int q = warp - 4;
         const int p = 32 * q + lane;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        // thread p's 112-byte record straight from the pool into registers,
-        // a tile ahead (7 x 16-byte read-only loads)
-        auto fetch = [&](int i, uint32_t (&w)[24], uint32_t (&sc)[4]) {
-            const int pos0 = p_begin + i * kTileP;
-            const int32_t page = (i < n_tiles) ? tile_page(a, pt_row, pos0) : -1;
-            if (page >= 0 && pos0 + p < p_end) {
-                const uint4* r4 = reinterpret_cast<const uint4*>(
-                    a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, 0, pos0 % kPageSize + p));
+        if constexpr (FMT == kFmtFp8) {
+            // thread p's 256-byte E4M3 record, half (128 dims) at a time, the
+            // next half's 8 x 16-byte loads in flight while this one converts
+            auto fetch_half = [&](int i, int hh, uint32_t (&w)[32]) {
+                const int pos0 = p_begin + i * kTileP;
+                const int32_t page = (i < n_tiles) ? tile_page(a, pt_row, pos0) : -1;
+                if (page >= 0 && pos0 + p < p_end) {
+                    const uint4* r4 = reinterpret_cast<const uint4*>(
+                        a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, 0,
+                                               pos0 % kPageSize + p, kRecB)) + 8 * hh;
 #pragma unroll
-                for (int m = 0; m < 6; ++m) {
-                    const uint4 u = __ldg(r4 + m);
-                    w[4 * m] = u.x; w[4 * m + 1] = u.y; w[4 * m + 2] = u.z; w[4 * m + 3] = u.w;
+                    for (int m = 0; m < 8; ++m) {
+                        const uint4 u = __ldg(r4 + m);
+                        w[4 * m] = u.x; w[4 * m + 1] = u.y; w[4 * m + 2] = u.z; w[4 * m + 3] = u.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int m = 0; m < 32; ++m) w[m] = 0u;
                 }
-                const uint4 u = __ldg(r4 + 6);
-                sc[0] = u.x; sc[1] = u.y; sc[2] = u.z; sc[3] = u.w;
-            } else {
-#pragma unroll
-                for (int m = 0; m < 24; ++m) w[m] = 0u;
-                sc[0] = sc[1] = sc[2] = sc[3] = 0u;
-            }
-        };
-        uint32_t wn[24], sn[4];
-        fetch(0, wn, sn);
-        bool ok = true;
-        for (int i = 0; i < n_tiles; ++i) {
-            uint32_t w[24], sc[4];
-#pragma unroll
-            for (int m = 0; m < 24; ++m) w[m] = wn[m];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) sc[m] = sn[m];
-            fetch(i + 1, wn, sn);                    // the next tile's record is in flight meanwhile
-            const bool valid = ok && p_begin + i * kTileP + p < p_end;
-            // two halves of the dims, each after its QK half of the previous tile
+            };
+            uint32_t wn[32];
+            fetch_half(0, 0, wn);
+            bool ok = true;
+            for (int i = 0; i < n_tiles; ++i) {
 #pragma unroll 1
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t wh[12], sh[2];
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t w[32];
 #pragma unroll
-                for (int m = 0; m < 12; ++m) wh[m] = hh ? w[12 + m] : w[m];
-                sh[0] = hh ? sc[2] : sc[0];
-                sh[1] = hh ? sc[3] : sc[1];
-                if (i > 0) ok = ok && warp_wait(&bar.qk_done[hh], (uint32_t)((i - 1) & 1), abort);
-                tc_fence_after();
-                const uint32_t col = tmem + lane_base + 64 * hh;
+                    for (int m = 0; m < 32; ++m) w[m] = wn[m];
+                    fetch_half(hh ? i + 1 : i, hh ^ 1, wn);
+                    if (i > 0) ok = ok && warp_wait(&bar.qk_done[hh], (uint32_t)((i - 1) & 1), abort);
+                    tc_fence_after();
+                    const uint32_t col = tmem + lane_base + kColKHi + 64 * hh;
 #pragma unroll
-                for (int bb = 0; bb < 4; ++bb) {
-                    uint32_t hi[16], lo[16];
-                    const __half s = __ushort_as_half((unsigned short)((bb & 1) ? (sh[bb >> 1] >> 16) : (sh[bb >> 1] & 0xFFFFu)));
-                    dequant_block(&wh[3 * bb], s, hi, lo);
-                    range_bad |= valid && !(__half2float(s) <= kMaxScale);
-                    tmem_st16(col + kColKHi + 16 * bb, hi);
-                    tmem_st16(col + kColKLo + 16 * bb, lo);
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t h16[16];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) e4m3x4_to_f16(w[8 * c + k], h16[2 * k], h16[2 * k + 1]);
+                        tmem_st16(col + 16 * c, h16);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar.kready[hh]);
                 }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.kready[hh]);
+            }
+        } else {
+            // thread p's 112-byte record straight from the pool into registers,
+            // a tile ahead (7 x 16-byte read-only loads)
+            auto fetch = [&](int i, uint32_t (&w)[24], uint32_t (&sc)[4]) {
+                const int pos0 = p_begin + i * kTileP;
+                const int32_t page = (i < n_tiles) ? tile_page(a, pt_row, pos0) : -1;
+                if (page >= 0 && pos0 + p < p_end) {
+                    const uint4* r4 = reinterpret_cast<const uint4*>(
+                        a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, 0, pos0 % kPageSize + p));
+#pragma unroll
+                    for (int m = 0; m < 6; ++m) {
+                        const uint4 u = __ldg(r4 + m);
+                        w[4 * m] = u.x; w[4 * m + 1] = u.y; w[4 * m + 2] = u.z; w[4 * m + 3] = u.w;
+                    }
+                    const uint4 u = __ldg(r4 + 6);
+                    sc[0] = u.x; sc[1] = u.y; sc[2] = u.z; sc[3] = u.w;
+                } else {
+#pragma unroll
+                    for (int m = 0; m < 24; ++m) w[m] = 0u;
+                    sc[0] = sc[1] = sc[2] = sc[3] = 0u;
+                }
+            };
+            uint32_t wn[24], sn[4];
+            fetch(0, wn, sn);
+            bool ok = true;
+            for (int i = 0; i < n_tiles; ++i) {
+                uint32_t w[24], sc[4];
+#pragma unroll
+                for (int m = 0; m < 24; ++m) w[m] = wn[m];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) sc[m] = sn[m];
+                fetch(i + 1, wn, sn);                    // the next tile's record is in flight meanwhile
+                const bool valid = ok && p_begin + i * kTileP + p < p_end;
+                // two halves of the dims, each after its QK half of the previous tile
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t wh[12], sh[2];
+#pragma unroll
+                    for (int m = 0; m < 12; ++m) wh[m] = hh ? w[12 + m] : w[m];
+                    sh[0] = hh ? sc[2] : sc[0];
+                    sh[1] = hh ? sc[3] : sc[1];
+                    if (i > 0) ok = ok && warp_wait(&bar.qk_done[hh], (uint32_t)((i - 1) & 1), abort);
+                    tc_fence_after();
+                    const uint32_t col = tmem + lane_base + 64 * hh;
+#pragma unroll
+                    for (int bb = 0; bb < 4; ++bb) {
+                        uint32_t hi[16], lo[16];
+                        const __half s = __ushort_as_half((unsigned short)((bb & 1) ? (sh[bb >> 1] >> 16) : (sh[bb >> 1] & 0xFFFFu)));
+                        dequant_block(&wh[3 * bb], s, hi, lo);
+                        range_bad |= valid && !(__half2float(s) <= kMaxScale);
+                        tmem_st16(col + kColKHi + 16 * bb, hi);
+                        tmem_st16(col + kColKLo + 16 * bb, lo);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar.kready[hh]);
+                }
             }
         }
     } else if (warp < 12) {
@@ -914,16 +994,37 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                 const int k = u / kVBufs;
                 if (k >= 1) ok = ok && warp_wait(&bar.v_free[b], (uint32_t)((k - 1) & 1), abort);
                 __half* vh = sm.v[b][0];
-                __half* vl = sm.v[b][1];
-                const uint8_t* rb = sm.vrec + kRecordBytes * r0;
+                const uint8_t* rb = sm.vrec + kRecB * r0;
 #pragma unroll 1
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < 4 && FMT == kFmtFp8; ++j) {
+                    // 32 dims of one position: 32 E4M3 bytes -> 16 fp16 pairs (exact)
+                    const int pl = 8 * (j >> 1) + (lane & 7);
+                    const int blk = 4 * (j & 1) + (lane >> 3);
+                    uint4 u0 = make_uint4(0u, 0u, 0u, 0u), u1 = u0;
+                    if (ok && page_ok && pos0 + r0 + pl < p_end) {
+                        const uint4* r = reinterpret_cast<const uint4*>(rb + kRecB * pl + 32 * blk);
+                        u0 = r[0];
+                        u1 = r[1];
+                    }
+                    const uint32_t w8[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                    uint32_t h16[16];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) e4m3x4_to_f16(w8[k], h16[2 * k], h16[2 * k + 1]);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4*>(&vh[v_off(32 * blk + 8 * c, pl)]) =
+                            make_uint4(h16[4 * c], h16[4 * c + 1], h16[4 * c + 2], h16[4 * c + 3]);
+                }
+#pragma unroll 1
+                for (int j = 0; j < 4 && FMT == kFmtQ3; ++j) {
+                    __half* vl = sm.v[b][Fmt<FMT>::kLo ? 1 : 0];
+
                     const int pl = 8 * (j >> 1) + (lane & 7);
                     const int blk = 4 * (j & 1) + (lane >> 3);
                     uint32_t w3[3];
                     __half s = __ushort_as_half((unsigned short)0);
                     if (ok && page_ok && pos0 + r0 + pl < p_end) {
-                        const uint8_t* r = rb + kRecordBytes * pl;
+                        const uint8_t* r = rb + kRecB * pl;
                         const uint32_t* wp = reinterpret_cast<const uint32_t*>(r + 12 * blk);
                         w3[0] = wp[0]; w3[1] = wp[1]; w3[2] = wp[2];
                         s = *reinterpret_cast<const __half*>(r + 96 + 2 * blk);
@@ -947,8 +1048,8 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                 if (producer) {
                     mbar_arrive(&bar.v_ready[b]);
                     if (ok && i + 1 < n_tiles && !*abort) {
-                        issue_rec_copy(a, pt_row, g, 1, pos0 + kTileP, r0, kSubP, sm.vrec + kRecordBytes * r0,
-                                       &bar.vfull[q][e]);
+                        issue_rec_copy<kRecB>(a, pt_row, g, 1, pos0 + kTileP, r0, kSubP, sm.vrec + kRecB * r0,
+                                              &bar.vfull[q][e]);
                         pend[e] = i + 1;
                     }
                 }
@@ -982,7 +1083,7 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                 if (elect_one()) {
                     mma_ts(dS, aK_hi + 8 * j, bq_hi + ko, idesc_qk, (h == 0 && j == 0) ? 0u : 1u);
                     mma_ts(dS, aK_hi + 8 * j, bq_lo + ko, idesc_qk, 1u);
-                    mma_ts(dS, aK_lo + 8 * j, bq_hi + ko, idesc_qk, 1u);
+                    if (Fmt<FMT>::kLo) mma_ts(dS, aK_lo + 8 * j, bq_hi + ko, idesc_qk, 1u);
                 }
                 __syncwarp();
             }
@@ -1002,7 +1103,8 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         const uint64_t bp_lo0 = make_desc(smem_u32(sm.plo[0]), kPLbo, kPSbo);
         const uint64_t pbuf = (uint64_t)(sizeof(sm.phi[0]) >> 4);    // one P^T buffer, 16-byte units
         const uint64_t av_hi0 = make_desc(smem_u32(sm.v[0][0]) + (uint32_t)(16 * h) * kVSbo, kVLbo, kVSbo);
-        const uint64_t av_lo0 = make_desc(smem_u32(sm.v[0][1]) + (uint32_t)(16 * h) * kVSbo, kVLbo, kVSbo);
+        const uint64_t av_lo0 =
+            make_desc(smem_u32(sm.v[0][Fmt<FMT>::kLo ? 1 : 0]) + (uint32_t)(16 * h) * kVSbo, kVLbo, kVSbo);
         const uint64_t vbuf = (uint64_t)(sizeof(sm.v[0]) >> 4);      // one V buffer, 16-byte units
         for (int jt = 0; jt < n_tiles; ++jt) {
             const int pb = jt & 1;
@@ -1023,7 +1125,7 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                 const uint64_t avh = av_hi0 + bfo, avl = av_lo0 + bfo, bph = bp_hi0 + koff, bpl = bp_lo0 + koff;
                 if (elect_one()) {
                     mma_ss(dO, avh, bph, idesc_pv, acc0);
-                    mma_ss(dO, avl, bph, idesc_pv, 1u);
+                    if (Fmt<FMT>::kLo) mma_ss(dO, avl, bph, idesc_pv, 1u);
                     mma_ss(dO, avh, bpl, idesc_pv, 1u);
                     mma_commit(&bar.v_free[b]);
                 }
@@ -1047,21 +1149,22 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         return;
     }
     if (n_splits == 1) {
-        rotate_rows(outs, Rc);
+        if (Fmt<FMT>::kRot) rotate_rows(outs, Rc);
+        constexpr float kOutScale = Fmt<FMT>::kRot ? 0.0625f : 1.0f;   // unnormalised H: 1/16
         for (int idx = tid; idx < Rc * kHeadDim; idx += kThreads) {
             const int r = idx / kHeadDim, dd = idx % kHeadDim;
             const int ra = row0 + r;
-            a.out[((q_base + ra / kGroup) * Hq + g * kGroup + ra % kGroup) * kHeadDim + dd] = outs[idx] * 0.0625f;
+            a.out[((q_base + ra / kGroup) * Hq + g * kGroup + ra % kGroup) * kHeadDim + dd] = outs[idx] * kOutScale;
         }
     }
 }
 
-template <typename TIn>
+template <typename TIn, int FMT>
 cudaError_t launch_typed(const VerifyArgs& a, cudaStream_t stream, bool& attr_set) {
-    const size_t smem = sizeof(MmaSmem);
+    const size_t smem = sizeof(MmaSmem<FMT>);
     if (!attr_set) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(verify_mma_kernel<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        const cudaError_t e = cudaFuncSetAttribute(verify_mma_kernel<TIn, FMT>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -1076,7 +1179,7 @@ cudaError_t launch_typed(const VerifyArgs& a, cudaStream_t stream, bool& attr_se
         qc.stream = stream;
         qc.attrs = attr;
         qc.numAttrs = 1;
-        const cudaError_t e = cudaLaunchKernelEx(&qc, qprep_kernel<TIn>, a);
+        const cudaError_t e = cudaLaunchKernelEx(&qc, qprep_kernel<TIn, Fmt<FMT>::kRot>, a);
         if (e != cudaSuccess) return e;
     }
     // the verify grid may start while the query kernel runs: only its QK
@@ -1088,17 +1191,21 @@ cudaError_t launch_typed(const VerifyArgs& a, cudaStream_t stream, bool& attr_se
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, verify_mma_kernel<TIn>, a);
+    return cudaLaunchKernelEx(&cfg, verify_mma_kernel<TIn, FMT>, a);
 }
 
 }  // namespace
 
 cudaError_t launch_verify_mma(const VerifyArgs& a, cudaStream_t stream) {
-    static bool attr_set[2] = {false, false};
-    if (a.dtype == Q3KV_F32) return launch_typed<float>(a, stream, attr_set[0]);
-    return launch_typed<__nv_bfloat16>(a, stream, attr_set[1]);
+    static bool attr_set[4] = {false, false, false, false};
+    const bool f32 = a.dtype == Q3KV_F32;
+    if (a.fmt == kFmtFp8)
+        return f32 ? launch_typed<float, kFmtFp8>(a, stream, attr_set[2])
+                   : launch_typed<__nv_bfloat16, kFmtFp8>(a, stream, attr_set[3]);
+    return f32 ? launch_typed<float, kFmtQ3>(a, stream, attr_set[0])
+               : launch_typed<__nv_bfloat16, kFmtQ3>(a, stream, attr_set[1]);
 }
 
-size_t verify_mma_smem_bytes() { return sizeof(MmaSmem); }
+size_t verify_mma_smem_bytes() { return sizeof(MmaSmem<kFmtQ3>); }
 
 }  // namespace q3kv

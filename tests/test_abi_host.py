@@ -149,3 +149,18 @@ def test_accept_argument_checks():
     assert lib.q3kv_accept_greedy(*wide) == _lib.Q3KV_ERR_UNSUPPORTED
     many_rows = list(args); many_rows[8] = 70000
     assert lib.q3kv_accept_greedy(*many_rows) == _lib.Q3KV_ERR_UNSUPPORTED
+
+
+def test_fp8_argument_checks(lib):
+    d = api.make_desc(2, 2, 4)
+    n = ctypes.c_size_t()
+    assert lib.q3kv_fp8_pool_bytes(ctypes.byref(d), ctypes.byref(n)) == 0
+    assert n.value == 4 * 2 * 2 * 2 * 256 * 256            # 256-byte records
+    assert lib.q3kv_fp8_append(None, ctypes.byref(d), None, None, 4, None, None, None, 0, 0, 0, None, None, 0,
+                               None) == 0
+    assert lib.q3kv_fp8_append(None, ctypes.byref(d), None, None, 4, None, None, None, 1, 1, 2, None, None, 0,
+                               None) == -1
+    # the CUDA-core leg does not read this format
+    args = [None, ctypes.byref(d), None, None, 4, None, None, None, 1, 1000, 4, 0, None, 0, None,
+            _lib.Q3KV_IMPL_FMA, 256, None, 0, None]
+    assert lib.q3kv_fp8_verify_attn(*args) == _lib.Q3KV_ERR_UNSUPPORTED
