@@ -145,3 +145,75 @@ def sample_accept(logits: np.ndarray, q_offsets, n_q, tokens, ctx_len, tau: floa
         nxt[b] = int(np.argmax(keys))
         committed[b] = int(ctx_len[b]) - (T - 1 - a)
     return n_acc, nxt, committed
+
+
+# ----------------------------------------------------------------------------- top-p nucleus
+# The pages' sampled speculative decode filters each target distribution to its
+# top-p nucleus before the Gumbel-max draw and the rejection test ("Model tool
+# protocol" bullet), on the temperature-scaled distribution (the sampler
+# paragraph of "Serving": q27 filters after temperature).  Reading taken here,
+# a threshold rule on the logits (the pages do not say how ties at the cut are
+# broken; this keeps all of them):
+#
+# * p_j = softmax(l_j / tau); for a logit value t, mass(t) = sum of p_j(x) over
+#   the tokens with l_x >= t;
+# * l* = the largest logit value of the row with mass(l*) >= top_p; the nucleus
+#   is {x : l_x >= l*} (every token tied with the cut is in);
+# * the filtered distribution is p_j restricted to the nucleus, renormalised;
+#   top_p >= 1 keeps every token (the plain sampled acceptance).
+# The draft test, the residual and the bonus draw are those of sample_accept
+# with the filtered distribution: a draft outside the nucleus is always
+# rejected, and the Gumbel-max argmax runs over the nucleus only.
+
+
+def nucleus_cut(logits_row: np.ndarray, tau: float, top_p: float):
+    """(l*, mass of the nucleus) of one row; l* = -inf keeps every token."""
+    l = np.asarray(logits_row, np.float64)
+    p = np.exp(l / tau - np.max(l / tau))
+    p /= p.sum()
+    if top_p >= 1.0:
+        return -np.inf, 1.0
+    vals = np.unique(l)[::-1]                          # distinct logits, largest first
+    for t in vals:
+        m = float(p[l >= t].sum())
+        if m >= top_p:
+            return float(t), m
+    return float(vals[-1]), 1.0
+
+
+def sample_accept_nucleus(logits: np.ndarray, q_offsets, n_q, tokens, ctx_len, tau: float, top_p: float,
+                          uniforms, seed: int):
+    """Rejection-sampled acceptance with top-p nucleus filtering; returns (n_accepted, next_token, committed_len)."""
+    S = len(n_q)
+    n_acc = np.zeros(S, np.int32)
+    nxt = np.full(S, -1, np.int32)
+    committed = np.array(ctx_len, np.int64).astype(np.int32)
+    V = logits.shape[1]
+    for b in range(S):
+        T = int(n_q[b])
+        if T <= 0:
+            continue
+        r0 = int(q_offsets[b])
+
+        def filtered_prob(j, d):
+            row = np.asarray(logits[r0 + j], np.float64)
+            cut, mass = nucleus_cut(row, tau, top_p)
+            if not (0 <= d < V) or row[d] < cut:
+                return 0.0
+            return target_prob(row, tau, d) / mass
+
+        a = 0
+        while a < T - 1 and float(uniforms[r0 + a]) < filtered_prob(a, int(tokens[r0 + a + 1])):
+            a += 1
+        row = np.asarray(logits[r0 + a], np.float64)
+        cut, _ = nucleus_cut(row, tau, top_p)
+        keys = gumbel_keys(row, tau, seed, r0 + a)
+        keys[row < cut] = -np.inf
+        if a < T - 1:
+            d = int(tokens[r0 + a + 1])
+            if 0 <= d < V:
+                keys[d] = -np.inf
+        n_acc[b] = a
+        nxt[b] = int(np.argmax(keys))
+        committed[b] = int(ctx_len[b]) - (T - 1 - a)
+    return n_acc, nxt, committed

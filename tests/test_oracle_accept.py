@@ -161,3 +161,81 @@ def test_low_temperature_reduces_to_greedy():
     got = sample_accept(lg, offs, nq, toks, ctx, 1e-4, u, seed=1)
     for w_, g_ in zip(want, got):
         assert np.array_equal(w_, g_)
+
+
+# ----------------------------------------------------------------------------- top-p nucleus
+from oracle.accept import nucleus_cut, sample_accept_nucleus
+
+
+def test_nucleus_hand_cases():
+    lg = np.log(np.array([0.5, 0.3, 0.2]))
+    assert nucleus_cut(lg, 1.0, 0.6) == (lg[1], pytest.approx(0.8))       # {0, 1}
+    assert nucleus_cut(lg, 1.0, 0.5)[0] == lg[0]                           # {0}: 0.5 >= 0.5
+    assert nucleus_cut(lg, 1.0, 0.81)[0] == lg[2]                          # everything
+    assert nucleus_cut(lg, 1.0, 1.0)[0] == -np.inf
+    # ties at the cut are all kept
+    cut, mass = nucleus_cut(np.array([1.0, 1.0, 0.0, 0.0, -1.0]), 1.0, 0.1)
+    assert cut == 1.0 and mass == pytest.approx(2 * np.e / (2 * np.e + 2 + np.exp(-1)))
+
+
+def test_nucleus_matches_sorted_prefix_without_ties():
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        V = int(rng.integers(2, 60))
+        l = rng.standard_normal(V) * 2
+        tau = float(rng.uniform(0.3, 2.0))
+        top_p = float(rng.uniform(0.05, 0.99))
+        p = np.exp(l / tau - np.max(l / tau))
+        p /= p.sum()
+        order = np.argsort(-l, kind="stable")
+        c = np.cumsum(p[order])
+        k = int(np.searchsorted(c, top_p))              # first prefix reaching top_p
+        want = set(order[: min(k, V - 1) + 1].tolist())
+        cut, mass = nucleus_cut(l, tau, top_p)
+        got = set(np.flatnonzero(l >= cut).tolist())
+        assert got == want
+        assert abs(mass - p[list(got)].sum()) < 1e-12
+
+
+def test_nucleus_acceptance_hand_case():
+    # row 0: p = (0.5, 0.3, 0.2), top_p 0.6 -> q = (0.625, 0.375, 0)
+    lg = np.log(np.array([[0.5, 0.3, 0.2], [0.2, 0.3, 0.5]]))
+    run = lambda toks, u: sample_accept_nucleus(lg, [0], [2], np.array(toks), [7], 1.0, 0.6, np.array([u, 0.5]), 11)
+    a, n, c = run([0, 1], 0.37)
+    assert int(a[0]) == 1 and int(c[0]) == 7 and int(n[0]) in (1, 2)      # accepted; bonus from row 1's nucleus {2, 1}
+    a, n, c = run([0, 1], 0.38)
+    assert (int(a[0]), int(n[0]), int(c[0])) == (0, 0, 6)                 # rejected: the residual nucleus is {0}
+    a, n, c = run([0, 2], 1e-9)
+    assert int(a[0]) == 0 and int(n[0]) in (0, 1)                          # outside the nucleus: always rejected
+
+
+def test_top_p_one_is_plain_sampling():
+    rng = np.random.default_rng(6)
+    nq = [4, 0, 6, 1]
+    offs = np.concatenate([[0], np.cumsum(nq)[:-1]])
+    rows = sum(nq)
+    lg = rng.standard_normal((rows, 40))
+    toks = rng.integers(0, 40, size=rows).astype(np.int32)
+    u = rng.uniform(0.001, 0.999, size=rows)
+    ctx = [10, 20, 30, 40]
+    want = sample_accept(lg, offs, nq, toks, ctx, 0.8, u, seed=2)
+    got = sample_accept_nucleus(lg, offs, nq, toks, ctx, 0.8, 1.0, u, seed=2)
+    for w_, g_ in zip(want, got):
+        assert np.array_equal(w_, g_)
+
+
+def test_gumbel_max_over_the_nucleus_samples_the_filtered_distribution():
+    lg = np.array([1.0, 0.0, -1.0, 2.0, 0.5, -3.0])
+    tau, top_p = 0.9, 0.7
+    cut, mass = nucleus_cut(lg, tau, top_p)
+    p = np.exp(lg / tau - np.max(lg / tau))
+    p /= p.sum()
+    q = np.where(lg >= cut, p, 0.0) / mass
+    counts = np.zeros(6)
+    n = 40000
+    for row in range(n):
+        keys = gumbel_keys(lg, tau, 5, row)
+        keys[lg < cut] = -np.inf
+        counts[int(np.argmax(keys))] += 1
+    assert np.max(np.abs(counts / n - q)) < 0.012
+    assert counts[lg < cut].sum() == 0
