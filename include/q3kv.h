@@ -286,7 +286,7 @@ Q3KV_API int q3kv_accept_greedy(void* stream, const void* logits, int32_t dtype,
  * Source: "Quasar" (q27) wiki, "Model tool protocol" bullet: temperature > 0
  * routes to sampled speculative decode with Gumbel-max sampling and
  * rejection-sampled acceptance, seeded and reproducible.  This call's reading
- * (the pages' top-p nucleus filter is not built): the drafts are point masses
+ * (without the top-p nucleus; see q3kv_accept_sample_nucleus): the drafts are point masses
  * (a deterministic drafter), p_j = softmax(logits row j / temperature), and
  *   draft d_{j+1} is accepted iff d_uniforms[row j] < p_j(d_{j+1});
  *   at the first rejected row a, next = argmax over x != d_{a+1} of
@@ -308,6 +308,32 @@ Q3KV_API int q3kv_accept_sample(void* stream, const void* logits, int32_t dtype,
                        const int32_t* d_q_offsets, const int32_t* d_n_q, const int32_t* d_tokens,
                        int32_t num_slots, int32_t num_rows, int32_t max_n_q, const int32_t* d_ctx_len,
                        float temperature, const float* d_uniforms, uint64_t seed,
+                       int32_t* d_n_accepted, int32_t* d_next_token, int32_t* d_committed_len,
+                       void* d_workspace, size_t workspace_bytes, int32_t* d_status);
+
+/* ---- sampled acceptance with the top-p nucleus ---------------------------------
+ * Source: the same "Model tool protocol" bullet (sampled speculative decode
+ * filters with a top-p nucleus before the Gumbel-max draw and the rejection
+ * test) and the sampler paragraph of "Serving" (the nucleus is taken on the
+ * temperature-scaled distribution).  Reading: the nucleus of row j is
+ * {x : logits_j[x] >= l*}, l* the largest logit of the row whose tokens at or
+ * above it carry at least top_p of p_j = softmax(logits_j / temperature) (all
+ * tokens tied with the cut are kept); q_j = p_j restricted to the nucleus and
+ * renormalised.  Then exactly q3kv_accept_sample's rule with q_j for p_j: draft
+ * d_{j+1} is accepted iff d_uniforms[row j] < q_j(d_{j+1}) (0 outside the
+ * nucleus), and the residual / bonus argmax of logits / temperature + G runs
+ * over the nucleus only (without the rejected token).
+ *   top_p   in (0, 1]; 1 gives q3kv_accept_sample's result (else
+ *           Q3KV_ERR_INVALID_ARG)
+ * The cut is found by a radix select over the logits' order (masses summed
+ * in 2^-40 fixed point, so the search is deterministic); results equal the
+ * float64 definition except where top_p, a uniform or a key lies within
+ * rounding of a tie.  Same arguments, outputs, workspace and errors as
+ * q3kv_accept_sample. */
+Q3KV_API int q3kv_accept_sample_nucleus(void* stream, const void* logits, int32_t dtype, int32_t vocab,
+                       const int32_t* d_q_offsets, const int32_t* d_n_q, const int32_t* d_tokens,
+                       int32_t num_slots, int32_t num_rows, int32_t max_n_q, const int32_t* d_ctx_len,
+                       float temperature, float top_p, const float* d_uniforms, uint64_t seed,
                        int32_t* d_n_accepted, int32_t* d_next_token, int32_t* d_committed_len,
                        void* d_workspace, size_t workspace_bytes, int32_t* d_status);
 

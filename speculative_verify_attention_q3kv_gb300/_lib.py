@@ -82,6 +82,10 @@ PROTOTYPES = {
                                      c_int32, c_int32, c_int32, c_void_p, ctypes.c_float, c_void_p,
                                      ctypes.c_uint64, c_void_p, c_void_p, c_void_p, c_void_p, ctypes.c_size_t,
                                      c_void_p]),
+    "q3kv_accept_sample_nucleus": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
+                                             c_int32, c_int32, c_int32, c_void_p, ctypes.c_float, ctypes.c_float,
+                                             c_void_p, ctypes.c_uint64, c_void_p, c_void_p, c_void_p, c_void_p,
+                                             ctypes.c_size_t, c_void_p]),
 }
 
 Q3KV_NOALLOC_SCRATCH_BYTES = 16 << 20

@@ -217,3 +217,22 @@ def accept_sample(logits: torch.Tensor, q_offsets: torch.Tensor, n_q: torch.Tens
                                         _ptr(n_accepted), _ptr(next_token), _ptr(committed_len), _ptr(workspace),
                                         nbytes, _ptr(status))
     check(rc, "q3kv_accept_sample")
+
+
+def accept_sample_nucleus(logits: torch.Tensor, q_offsets: torch.Tensor, n_q: torch.Tensor, tokens: torch.Tensor,
+                          max_n_q: int, ctx_len: torch.Tensor, temperature: float, top_p: float,
+                          uniforms: torch.Tensor, seed: int, n_accepted: torch.Tensor, next_token: torch.Tensor,
+                          committed_len: torch.Tensor, workspace: Optional[torch.Tensor],
+                          status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """q3kv_accept_sample_nucleus: rejection-sampled acceptance with the top-p nucleus."""
+    rows, vocab = logits.shape
+    if uniforms.dtype != torch.float32:
+        raise TypeError("uniforms must be float32")
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = _lib.load().q3kv_accept_sample_nucleus(_stream(stream), _ptr(logits), _dtype_code(logits), vocab,
+                                                _ptr(q_offsets), _ptr(n_q), _ptr(tokens), n_q.shape[0], rows,
+                                                max_n_q, _ptr(ctx_len), float(temperature), float(top_p),
+                                                _ptr(uniforms), int(seed) & ((1 << 64) - 1), _ptr(n_accepted),
+                                                _ptr(next_token), _ptr(committed_len), _ptr(workspace), nbytes,
+                                                _ptr(status))
+    check(rc, "q3kv_accept_sample_nucleus")

@@ -352,3 +352,269 @@ cudaError_t launch_accept_sample(const AcceptArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace q3kv
+
+// ---------------------------------------------------------------------------
+// Top-p nucleus for the sampled acceptance.
+//
+// Source: "Quasar" (q27 wiki), "Model tool protocol" bullet (sampled
+// speculative decode: top-p nucleus, Gumbel-max, rejection-sampled
+// acceptance) and the sampler paragraph of "Serving" (the nucleus is taken on
+// the temperature-scaled distribution).  Reading: the nucleus of row j is
+// {x : l_x >= l*}, l* the largest logit of the row whose tokens at or above it
+// carry at least top_p of softmax(l / tau) -- every token tied with the cut is
+// kept.
+//
+// The cut is found by a radix select over the logits' order keys, 8 bits per
+// level from the top (4 levels for f32 logits, 2 for bf16, whose low 16 bits
+// are zero): each level histograms the probability mass of the tokens that
+// match the prefix found so far, and a one-CTA-per-row step picks the bin where
+// the mass counted from the top first reaches top_p of the total.  Masses are
+// 2^-40 fixed point (each e^(l/tau - max) <= 1), so the sums are exact integers
+// whatever the order of the atomic adds: the search is deterministic.
+namespace q3kv {
+namespace {
+
+constexpr double kFixScale = 1099511627776.0;   // 2^40
+
+struct NucleusRow {
+    float m;                       // max of l / tau
+    uint32_t prefix;               // order-key bits of the cut found so far
+    unsigned long long above;      // mass of the tokens above the prefix's key range
+    unsigned long long target;     // ceil(top_p * total mass)
+    unsigned long long zn;         // mass of the nucleus (after the last level)
+    uint32_t key_star;             // order key of l*
+};
+static_assert(sizeof(NucleusRow) <= kNucleusRowBytes, "nucleus row");
+
+// Monotone key of a logit value (-0 taken as +0, so equal values get equal keys).
+__device__ __forceinline__ uint32_t order_key(float l) {
+    const uint32_t u = __float_as_uint(l == 0.0f ? 0.0f : l);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ NucleusRow* nrow(const AcceptArgs& a, int row) {
+    return reinterpret_cast<NucleusRow*>(static_cast<uint8_t*>(a.nucleus) + (size_t)row * kNucleusRowBytes);
+}
+__device__ __forceinline__ unsigned long long* nhist(const AcceptArgs& a, int row) {
+    return reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(a.nucleus) + (size_t)a.num_rows * kNucleusRowBytes +
+                                                 (size_t)row * kNucleusHistBytes);
+}
+
+// Per (chunk, row): max of l / tau (into the chunk partial's m), NaN flag.
+template <typename T>
+__global__ void __launch_bounds__(kArgThreads) nucleus_max_kernel(AcceptArgs a) {
+    __shared__ float red[kArgThreads / 32];
+    const int row = blockIdx.y, chunk = blockIdx.x;
+    const int64_t c0 = (int64_t)chunk * a.chunk_elems;
+    const int64_t c1 = min((int64_t)a.vocab, c0 + a.chunk_elems);
+    const T* lg = static_cast<const T*>(a.logits) + (int64_t)row * a.vocab;
+    float m = -CUDART_INF_F;
+    bool nan = false;
+    for (int64_t k = c0 + threadIdx.x; k < c1; k += kArgThreads) {
+        const float l = to_f(lg[k]) * a.inv_tau;
+        nan |= (l != l);
+        m = fmaxf(m, l);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (__any_sync(0xffffffffu, nan) && (threadIdx.x & 31) == 0 && a.status) atomicOr(a.status, Q3KV_STATUS_NONFINITE_INPUT);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kArgThreads / 32; ++w) m = fmaxf(m, red[w]);
+        SampleStat st = stat_empty();
+        st.m = m;
+        reinterpret_cast<SampleStat*>(a.partial)[(int64_t)row * a.num_chunks + chunk] = st;
+    }
+}
+
+// One CTA per row: the row maximum; clears the level-0 histogram.
+__global__ void __launch_bounds__(256) nucleus_init_kernel(AcceptArgs a) {
+    const int row = blockIdx.x;
+    __shared__ float red[8];
+    const SampleStat* pp = reinterpret_cast<const SampleStat*>(a.partial) + (int64_t)row * a.num_chunks;
+    float m = -CUDART_INF_F;
+    for (int k = threadIdx.x; k < a.num_chunks; k += 256) m = fmaxf(m, pp[k].m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    nhist(a, row)[threadIdx.x] = 0ull;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
+        NucleusRow* r = nrow(a, row);
+        r->m = m;
+        r->prefix = 0u;
+        r->above = 0ull;
+        r->target = 0ull;
+        r->zn = 0ull;
+        r->key_star = 0u;
+    }
+}
+
+// Per (chunk, row): fixed-point mass histogram of the next 8 key bits of the
+// tokens whose higher bits equal the prefix.
+template <typename T>
+__global__ void __launch_bounds__(kArgThreads) nucleus_hist_kernel(AcceptArgs a, int level) {
+    __shared__ unsigned long long h[256];
+    const int row = blockIdx.y, chunk = blockIdx.x;
+    h[threadIdx.x] = 0ull;
+    __syncthreads();
+    const NucleusRow* r = nrow(a, row);
+    const float m = r->m;
+    const uint32_t prefix = r->prefix;
+    const int shift = 24 - 8 * level;
+    const int64_t c0 = (int64_t)chunk * a.chunk_elems;
+    const int64_t c1 = min((int64_t)a.vocab, c0 + a.chunk_elems);
+    const T* lg = static_cast<const T*>(a.logits) + (int64_t)row * a.vocab;
+    for (int64_t k = c0 + threadIdx.x; k < c1; k += kArgThreads) {
+        const float raw = to_f(lg[k]);
+        const uint32_t key = order_key(raw);
+        if (level > 0 && (key >> (shift + 8)) != prefix) continue;
+        const unsigned long long mass = __double2ull_rn((double)__expf(raw * a.inv_tau - m) * kFixScale);
+        if (mass) atomicAdd(&h[(key >> shift) & 0xFFu], mass);
+    }
+    __syncthreads();
+    if (h[threadIdx.x]) atomicAdd(&nhist(a, row)[threadIdx.x], h[threadIdx.x]);
+}
+
+// One CTA per row: the bin where the mass counted from the top first reaches
+// the target; extends the prefix; clears the histogram for the next level.
+__global__ void __launch_bounds__(256) nucleus_select_kernel(AcceptArgs a, int level, int last) {
+    const int row = blockIdx.x;
+    __shared__ unsigned long long h[256];
+    unsigned long long* gh = nhist(a, row);
+    h[threadIdx.x] = gh[threadIdx.x];
+    __syncthreads();
+    gh[threadIdx.x] = 0ull;
+    if (threadIdx.x != 0) return;
+    NucleusRow* r = nrow(a, row);
+    if (level == 0) {
+        unsigned long long total = 0ull;
+        for (int b = 0; b < 256; ++b) total += h[b];
+        double t = ceil((double)a.top_p * (double)total);
+        r->target = t < (double)total ? (unsigned long long)t : total;
+    }
+    const unsigned long long target = r->target;
+    unsigned long long cum = r->above;
+    int sel = 0;
+    for (int b = 255; b >= 0; --b) {
+        if (cum + h[b] >= target) {
+            sel = b;
+            break;
+        }
+        cum += h[b];
+    }
+    r->prefix = (r->prefix << 8) | (uint32_t)sel;
+    r->above = cum;
+    if (last) {
+        r->key_star = r->prefix << (24 - 8 * level);   // bf16 stops after two levels: low bits of the key are the same
+        r->zn = cum + h[sel];
+    }
+}
+
+// Per (chunk, row): Gumbel-max candidates over the nucleus (overall and
+// without the row's next query token).
+template <typename T>
+__global__ void __launch_bounds__(kArgThreads) nucleus_gumbel_kernel(AcceptArgs a, uint32_t low_fill) {
+    __shared__ SampleStat red[kArgThreads / 32];
+    const int row = blockIdx.y, chunk = blockIdx.x;
+    const int64_t c0 = (int64_t)chunk * a.chunk_elems;
+    const int64_t c1 = min((int64_t)a.vocab, c0 + a.chunk_elems);
+    const T* lg = static_cast<const T*>(a.logits) + (int64_t)row * a.vocab;
+    const int excl = row + 1 < a.num_rows ? a.tokens[row + 1] : -1;
+    const uint32_t key_star = nrow(a, row)->key_star | low_fill;
+    SampleStat st = stat_empty();
+    for (int64_t k = c0 + threadIdx.x; k < c1; k += kArgThreads) {
+        const float raw = to_f(lg[k]);
+        if ((order_key(raw) | low_fill) < key_star) continue;
+        const float key = raw * a.inv_tau - logf(-logf(noise_uniform(a.seed, (uint32_t)row, (uint32_t)k)));
+        if (beats(key, (int)k, st.k1, st.i1)) { st.k1 = key; st.i1 = (int)k; }
+        if ((int)k != excl && beats(key, (int)k, st.k2, st.i2)) { st.k2 = key; st.i2 = (int)k; }
+    }
+    st = stat_warp(st);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = st;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        SampleStat c = threadIdx.x < kArgThreads / 32 ? red[threadIdx.x] : stat_empty();
+        c = stat_warp(c);
+        if (threadIdx.x == 0) reinterpret_cast<SampleStat*>(a.partial)[(int64_t)row * a.num_chunks + chunk] = c;
+    }
+}
+
+// One warp per slot: the draft tests against the filtered distribution, then
+// the residual or bonus candidate.
+template <typename TIn>
+__global__ void __launch_bounds__(32) nucleus_accept_kernel(AcceptArgs a, uint32_t low_fill) {
+    const int b = blockIdx.x, lane = threadIdx.x;
+    const int T = a.n_q[b];
+    const int32_t L = a.ctx_len[b];
+    if (T <= 0 || T > a.max_n_q || T > L || a.q_offsets[b] < 0 || a.q_offsets[b] + T > a.num_rows) {
+        if (lane == 0) {
+            if (T != 0 && a.status) atomicOr(a.status, Q3KV_STATUS_BAD_LENGTH);
+            a.n_accepted[b] = 0;
+            a.next_token[b] = -1;
+            a.committed_len[b] = L;
+        }
+        return;
+    }
+    const int r0 = a.q_offsets[b];
+    const int tok_next = lane + 1 < T ? a.tokens[r0 + lane + 1] : -1;
+    const float u = lane < T ? a.uniforms[r0 + lane] : 1.0f;
+    float p = 0.0f;
+    if (lane + 1 < T && tok_next >= 0 && tok_next < a.vocab) {
+        const NucleusRow* r = nrow(a, r0 + lane);
+        const float raw = to_f(static_cast<const TIn*>(a.logits)[(int64_t)(r0 + lane) * a.vocab + tok_next]);
+        if ((order_key(raw) | low_fill) >= (r->key_star | low_fill))
+            p = (float)((double)__expf(raw * a.inv_tau - r->m) * kFixScale / (double)r->zn);
+    }
+    const SampleStat* pp = reinterpret_cast<const SampleStat*>(a.partial) + (int64_t)r0 * a.num_chunks;
+    SampleStat mine = stat_empty();
+    for (int j = 0; j < T; ++j) {
+        SampleStat c = stat_empty();
+        for (int k = lane; k < a.num_chunks; k += 32) c = stat_merge(c, pp[(int64_t)j * a.num_chunks + k]);
+        c = stat_warp(c);
+        if (lane == j) mine = c;
+    }
+    const unsigned miss = __ballot_sync(0xffffffffu, lane + 1 < T && !(u < p));
+    const int acc = miss ? __ffs(miss) - 1 : T - 1;
+    const int cand = (acc < T - 1) ? mine.i2 : mine.i1;
+    const int nxt = __shfl_sync(0xffffffffu, cand, acc);
+    if (lane == 0) {
+        a.n_accepted[b] = acc;
+        a.next_token[b] = nxt;
+        a.committed_len[b] = L - (T - 1 - acc);
+    }
+}
+
+template <typename T>
+cudaError_t launch_nucleus_typed(const AcceptArgs& a, cudaStream_t stream) {
+    // bf16 logits: two levels of 8 key bits decide the value (the low 16 bits
+    // of every key are equal: 0 for positive values, all ones for negative
+    // ones; comparisons below fill them with ones so both read the same)
+    const int levels = (a.dtype == Q3KV_F32) ? 4 : 2;
+    const uint32_t low_fill = (a.dtype == Q3KV_F32) ? 0u : 0xFFFFu;
+    if (a.num_rows > 0) {
+        const dim3 grid((unsigned)a.num_chunks, (unsigned)a.num_rows);
+        nucleus_max_kernel<T><<<grid, kArgThreads, 0, stream>>>(a);
+        nucleus_init_kernel<<<a.num_rows, 256, 0, stream>>>(a);
+        for (int lv = 0; lv < levels; ++lv) {
+            nucleus_hist_kernel<T><<<grid, kArgThreads, 0, stream>>>(a, lv);
+            nucleus_select_kernel<<<a.num_rows, 256, 0, stream>>>(a, lv, lv == levels - 1 ? 1 : 0);
+        }
+        nucleus_gumbel_kernel<T><<<grid, kArgThreads, 0, stream>>>(a, low_fill);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    nucleus_accept_kernel<T><<<a.num_slots, 32, 0, stream>>>(a, low_fill);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_accept_nucleus(const AcceptArgs& a, cudaStream_t stream) {
+    if (a.dtype == Q3KV_F32) return launch_nucleus_typed<float>(a, stream);
+    return launch_nucleus_typed<__nv_bfloat16>(a, stream);
+}
+
+}  // namespace q3kv

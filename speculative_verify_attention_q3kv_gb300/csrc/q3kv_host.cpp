@@ -368,7 +368,8 @@ int q3kv_accept_workspace_bytes(int32_t num_rows, int32_t vocab, size_t* bytes) 
     int64_t chunk = 0;
     int e = accept_plan(num_rows, vocab, &nch, &chunk);
     if (e != Q3KV_OK) return e;
-    *bytes = (size_t)num_rows * (size_t)nch * kAcceptPartialBytes;
+    // the chunk partials, then (top-p nucleus) a row record and a 256-bin histogram per row
+    *bytes = (size_t)num_rows * ((size_t)nch * kAcceptPartialBytes + kNucleusRowBytes + kNucleusHistBytes);
     return Q3KV_OK;
 }
 
@@ -456,6 +457,60 @@ int q3kv_accept_sample(void* stream, const void* logits, int32_t dtype, int32_t 
     a.uniforms = d_uniforms;
     a.seed = seed;
     return cuda_status(launch_accept_sample(a, static_cast<cudaStream_t>(stream)));
+}
+
+int q3kv_accept_sample_nucleus(void* stream, const void* logits, int32_t dtype, int32_t vocab,
+                               const int32_t* d_q_offsets, const int32_t* d_n_q, const int32_t* d_tokens,
+                               int32_t num_slots, int32_t num_rows, int32_t max_n_q, const int32_t* d_ctx_len,
+                               float temperature, float top_p, const float* d_uniforms, uint64_t seed,
+                               int32_t* d_n_accepted, int32_t* d_next_token, int32_t* d_committed_len,
+                               void* d_workspace, size_t workspace_bytes, int32_t* d_status) {
+    if (!(top_p > 0.0f) || !(top_p <= 1.0f)) return Q3KV_ERR_INVALID_ARG;
+    if (top_p >= 1.0f)   // the nucleus is the whole vocabulary
+        return q3kv_accept_sample(stream, logits, dtype, vocab, d_q_offsets, d_n_q, d_tokens, num_slots, num_rows,
+                                  max_n_q, d_ctx_len, temperature, d_uniforms, seed, d_n_accepted, d_next_token,
+                                  d_committed_len, d_workspace, workspace_bytes, d_status);
+    if (dtype != Q3KV_F32 && dtype != Q3KV_BF16) return Q3KV_ERR_INVALID_ARG;
+    if (vocab <= 0 || num_slots < 0 || num_rows < 0 || max_n_q < 0) return Q3KV_ERR_INVALID_ARG;
+    if (!(temperature > 0.0f) || !(temperature < 3.0e38f)) return Q3KV_ERR_INVALID_ARG;
+    if (max_n_q > kMaxNq || num_rows > 65535 || num_slots > (1 << 30)) return Q3KV_ERR_UNSUPPORTED;
+    int32_t nch = 0;
+    int64_t chunk = 0;
+    int e = accept_plan(num_rows, vocab, &nch, &chunk);
+    if (e != Q3KV_OK) return e;
+    if (num_slots == 0) return Q3KV_OK;
+    if (!d_q_offsets || !d_n_q || !d_tokens || !d_ctx_len || !d_n_accepted || !d_next_token || !d_committed_len)
+        return Q3KV_ERR_INVALID_ARG;
+    if (num_rows > 0 && (!logits || !d_uniforms)) return Q3KV_ERR_INVALID_ARG;
+    const size_t part = (size_t)num_rows * (size_t)nch * kAcceptPartialBytes;
+    const size_t need = part + (size_t)num_rows * (kNucleusRowBytes + kNucleusHistBytes);
+    if (workspace_bytes < need || (need > 0 && !d_workspace)) return Q3KV_ERR_WORKSPACE_TOO_SMALL;
+    if (d_workspace && (reinterpret_cast<uintptr_t>(d_workspace) & 7u)) return Q3KV_ERR_INVALID_ARG;
+    AcceptArgs a{};
+    a.logits = logits;
+    a.dtype = dtype;
+    a.vocab = vocab;
+    a.chunk_elems = chunk;
+    a.num_chunks = nch;
+    a.vec_ok = 0;
+    a.q_offsets = d_q_offsets;
+    a.n_q = d_n_q;
+    a.tokens = d_tokens;
+    a.num_slots = num_slots;
+    a.num_rows = num_rows;
+    a.max_n_q = max_n_q;
+    a.ctx_len = d_ctx_len;
+    a.n_accepted = d_n_accepted;
+    a.next_token = d_next_token;
+    a.committed_len = d_committed_len;
+    a.partial = d_workspace;
+    a.status = d_status;
+    a.inv_tau = 1.0f / temperature;
+    a.uniforms = d_uniforms;
+    a.seed = seed;
+    a.top_p = top_p;
+    a.nucleus = d_workspace ? static_cast<void*>(static_cast<uint8_t*>(d_workspace) + part) : nullptr;
+    return cuda_status(launch_accept_nucleus(a, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -102,10 +102,17 @@ struct AcceptArgs {
     float inv_tau;             // 1 / temperature
     const float* uniforms;     // [num_rows] draft-test uniforms
     uint64_t seed;             // Gumbel noise stream
+    // top-p nucleus only
+    float top_p;
+    void* nucleus;             // [num_rows] NucleusRow, then [num_rows][256] u64 histograms
 };
+// Per-row scratch of the nucleus search (workspace, after the chunk partials).
+constexpr size_t kNucleusRowBytes = 64;
+constexpr size_t kNucleusHistBytes = 256 * 8;
 constexpr size_t kAcceptPartialBytes = 24;   // largest per-chunk record (sampled acceptance)
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t stream);
 cudaError_t launch_accept_sample(const AcceptArgs& a, cudaStream_t stream);
+cudaError_t launch_accept_nucleus(const AcceptArgs& a, cudaStream_t stream);
 
 // FMA (CUDA-core) leg: rows per CTA, and its workspace/launch.
 constexpr int kFmaRows = 64;

@@ -164,3 +164,11 @@ def test_fp8_argument_checks(lib):
     args = [None, ctypes.byref(d), None, None, 4, None, None, None, 1, 1000, 4, 0, None, 0, None,
             _lib.Q3KV_IMPL_FMA, 256, None, 0, None]
     assert lib.q3kv_fp8_verify_attn(*args) == _lib.Q3KV_ERR_UNSUPPORTED
+
+
+def test_nucleus_argument_checks(lib):
+    i = ctypes.c_int32(0)
+    p = ctypes.byref(i)
+    for top_p in (0.0, -0.5, 1.5, float("nan")):
+        assert lib.q3kv_accept_sample_nucleus(None, p, 0, 100, p, p, p, 1, 1, 1, p, 1.0, top_p, p, 1,
+                                              p, p, p, None, 0, None) == _lib.Q3KV_ERR_INVALID_ARG

@@ -211,3 +211,136 @@ def test_sample_accept_low_temperature_is_greedy():
     n_acc, nxt, com, st = _run_sample(logits, offs, nq, toks, ctx, False, 1e-3, u, 5)
     assert st == 0
     assert np.array_equal(n_acc, want[0]) and np.array_equal(nxt, want[1]) and np.array_equal(com, want[2])
+
+
+# ----------------------------------------------------------------------------- top-p nucleus
+from oracle.accept import nucleus_cut, sample_accept_nucleus
+
+
+def _run_nucleus(logits_np, offs, nq, toks, ctx, bf16, tau, top_p, u, seed):
+    from speculative_verify_attention_q3kv_gb300 import api
+    rows, vocab = logits_np.shape
+    lg = torch.from_numpy(logits_np).cuda()
+    if bf16:
+        lg = lg.to(torch.bfloat16)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    S = len(nq)
+    out = [torch.full((S,), -7, **i32) for _ in range(3)]
+    ws = torch.empty(max(api.accept_workspace_bytes(rows, vocab), 8), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, **i32)
+    api.accept_sample_nucleus(lg, torch.tensor(np.asarray(offs, np.int32), **i32),
+                              torch.tensor(np.asarray(nq, np.int32), **i32), torch.tensor(np.asarray(toks, np.int32), **i32),
+                              max(nq), torch.tensor(np.asarray(ctx, np.int32), **i32), tau, top_p,
+                              torch.from_numpy(np.asarray(u, np.float32)).cuda(), seed, *out, ws, st)
+    torch.cuda.synchronize()
+    return [o.cpu().numpy() for o in out] + [int(st.item())]
+
+
+def _clear_of_cut(lg64, tau, top_p, margin=1e-5):
+    """top_p is not within `margin` of a row's cumulative mass at its cut or just above it."""
+    for row in lg64:
+        p = np.exp(row / tau - np.max(row / tau))
+        p /= p.sum()
+        cut, mass = nucleus_cut(row, tau, top_p)
+        above = float(p[row > cut].sum())
+        if abs(mass - top_p) < margin or abs(top_p - above) < margin:
+            return False
+    return True
+
+
+@pytest.mark.parametrize("vocab", [1000, 50_257, qi.VOCAB])
+@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("top_p", [0.5, 0.9])
+def test_nucleus_accept_matches_oracle(vocab, bf16, top_p):
+    tau = 0.8
+    rng = np.random.default_rng(vocab + int(100 * top_p) + 7 * bf16)
+    nq = [int(x) for x in rng.integers(0, 17, size=8)]
+    nq[1], nq[5] = 0, 1
+    offs = np.concatenate([[0], np.cumsum(nq)[:-1]]).astype(np.int32)
+    rows = int(sum(nq))
+    # sharp rows (scale 4) so the nuclei are a few hundred tokens at most
+    logits = (qi.logits_rows(vocab + 5, rows, vocab, "normal", False) * 4.0).astype(np.float32)
+    if bf16:
+        logits = torch.from_numpy(logits).to(torch.bfloat16).float().numpy()
+    lg64 = logits.astype(np.float64)
+    while not _clear_of_cut(lg64, tau, top_p):
+        top_p = float(top_p + 1e-4)
+    toks = qi.random_tokens(vocab, rows, vocab)
+    top = np.argsort(-lg64, axis=1)[:, :4]
+    for b, T in enumerate(nq):
+        for j in range(1, T):
+            toks[offs[b] + j] = top[offs[b] + j - 1, int(rng.integers(0, 4))]
+    u = rng.uniform(0.0, 1.0, size=rows)
+    for b, T in enumerate(nq):
+        for j in range(T - 1):
+            r = offs[b] + j
+            cut, mass = nucleus_cut(lg64[r], tau, top_p)
+            d = int(toks[r + 1])
+            q = target_prob(lg64[r], tau, d) / mass if lg64[r, d] >= cut else 0.0
+            while abs(u[r] - q) < 2e-3:
+                u[r] = rng.uniform()
+    u = u.astype(np.float32)
+    ctx = [int(x) for x in rng.integers(20, 5000, size=8)]
+    seed = 0x0F0F_1234_5678_9ABC + vocab
+    want = sample_accept_nucleus(lg64, offs, nq, toks, ctx, tau, top_p, u.astype(np.float64), seed)
+    n_acc, nxt, com, st = _run_nucleus(logits, offs, nq, toks, ctx, bf16, tau, top_p, u, seed)
+    assert st == 0
+    assert np.array_equal(n_acc, want[0]) and np.array_equal(com, want[2])
+    for b, T in enumerate(nq):
+        if T == 0:
+            assert nxt[b] == -1
+            continue
+        r = offs[b] + int(n_acc[b])
+        cut, _ = nucleus_cut(lg64[r], tau, top_p)
+        assert lg64[r, nxt[b]] >= cut                   # always inside the nucleus
+        if nxt[b] == want[1][b]:
+            continue
+        keys = gumbel_keys(lg64[r], tau, seed, r)
+        keys[lg64[r] < cut] = -np.inf
+        if n_acc[b] < T - 1:
+            keys[int(toks[r + 1])] = -np.inf
+        assert keys[nxt[b]] >= keys.max() - 1e-4, (b, nxt[b], want[1][b])
+
+
+def test_nucleus_top_p_one_and_ties():
+    vocab = 3001
+    nq = [5, 4]
+    offs = [0, 5]
+    rows = 9
+    # values on a 0.5 grid: many exact ties, also at the cut
+    logits = (np.round(qi.logits_rows(17, rows, vocab, "normal", False) * 6) / 2).astype(np.float32)
+    lg64 = logits.astype(np.float64)
+    toks = qi.random_tokens(3, rows, vocab)
+    u = np.full(rows, 0.5, np.float32)
+    ctx = [40, 41]
+    # top_p = 1: the plain sampled acceptance
+    a1 = _run_nucleus(logits, offs, nq, toks, ctx, False, 1.0, 1.0, u, 9)
+    a0 = _run_sample(logits, offs, nq, toks, ctx, False, 1.0, u, 9)
+    for x, y in zip(a1, a0):
+        assert np.array_equal(x, y)
+    # ties at the cut are kept: the chosen token is in the oracle's (threshold) nucleus
+    for top_p in (0.05, 0.3):
+        while not _clear_of_cut(lg64, 1.0, top_p):
+            top_p += 1e-4
+        uu = u.copy()
+        for b, T in enumerate(nq):
+            for j in range(T - 1):
+                r = offs[b] + j
+                cut, mass = nucleus_cut(lg64[r], 1.0, top_p)
+                d = int(toks[r + 1])
+                q = target_prob(lg64[r], 1.0, d) / mass if lg64[r, d] >= cut else 0.0
+                if abs(uu[r] - q) < 2e-3:
+                    uu[r] = 0.9 if q < 0.5 else 0.1
+        n_acc, nxt, com, st = _run_nucleus(logits, offs, nq, toks, ctx, False, 1.0, top_p, uu, 9)
+        want = sample_accept_nucleus(lg64, offs, nq, toks, ctx, 1.0, top_p, uu.astype(np.float64), 9)
+        assert st == 0 and np.array_equal(n_acc, want[0]) and np.array_equal(com, want[2])
+        for b, T in enumerate(nq):
+            r = offs[b] + int(n_acc[b])
+            cut, _ = nucleus_cut(lg64[r], 1.0, top_p)
+            assert lg64[r, nxt[b]] >= cut
+            if nxt[b] != want[1][b]:
+                keys = gumbel_keys(lg64[r], 1.0, 9, r)
+                keys[lg64[r] < cut] = -np.inf
+                if n_acc[b] < T - 1:
+                    keys[int(toks[r + 1])] = -np.inf
+                assert keys[nxt[b]] >= keys.max() - 1e-4
