@@ -226,6 +226,7 @@ class Step:
         self.committed = torch.zeros(self.S, **i32)
         self.accept_ws = torch.empty(max(api.accept_workspace_bytes(self.rows, self.vocab), 8), dtype=torch.uint8,
                                      device=device)
+        self.uniforms = torch.rand(self.rows, generator=g, device=device)
         self._prefill(g)
 
     def _prefill(self, g):
@@ -270,6 +271,12 @@ class Step:
         """Greedy acceptance of the step's drafts and the committed lengths (once per step)."""
         self.api.accept_greedy(self.logits, self.row_off, self.n_new_d, self.tokens, self.max_new, self.ctx_len,
                                self.n_acc, self.next_tok, self.committed, self.accept_ws, self.status)
+
+    def accept_nucleus(self, temperature=1.0, top_p=0.95):
+        """Sampled acceptance with the top-p nucleus (the model card's temperature 1.0, top-p 0.95)."""
+        self.api.accept_sample_nucleus(self.logits, self.row_off, self.n_new_d, self.tokens, self.max_new,
+                                       self.ctx_len, temperature, top_p, self.uniforms, 1234, self.n_acc,
+                                       self.next_tok, self.committed, self.accept_ws, self.status)
 
     def launches_per_layer(self):
         """Our kernels per layer: append; for the tensor-core leg the query kernel and the verify
@@ -319,6 +326,7 @@ def run_ours(args, rank, world, local, pg):
     g_step = st.capture()
     g_verify = st.capture(append=False)
     g_accept = st.capture(st.accept)
+    g_nucleus = st.capture(st.accept_nucleus)
     for _ in range(max(args.warmup, 3)):
         g_step.replay()
         g_verify.replay()
@@ -347,11 +355,18 @@ def run_ours(args, rank, world, local, pg):
         aev[s][0].record(stream)
         g_accept.replay()                   # the step's acceptance (argmax + acceptance kernels)
         aev[s][1].record(stream)
+    nev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for s in range(args.steps):
+        flush.zero_()
+        nev[s][0].record(stream)
+        g_nucleus.replay()                  # sampled acceptance with the top-p nucleus
+        nev[s][1].record(stream)
     torch.cuda.synchronize()
     clock_info = clocks.stop()
     barrier(pg)
     step_ms = [a.elapsed_time(b_) for a, b_ in ev]
     accept_us = statistics.mean(a.elapsed_time(b_) for a, b_ in aev) * 1e3
+    nucleus_us = statistics.mean(a.elapsed_time(b_) for a, b_ in nev) * 1e3
     verify_ms = [a.elapsed_time(b_) / Ly for a, b_ in vev for _ in range(Ly)]   # per verify call
     total_s = max_over_ranks(pg, sum(step_ms) / 1e3)
     assert int(st.status.item()) == 0, "device status flagged during the benchmark"
@@ -426,7 +441,10 @@ def run_ours(args, rank, world, local, pg):
                      "mean_launch_us": mean_verify_s * 1e6},
         "accept": {"us": accept_us, "vocab": st.vocab, "logits_bytes": st.rows * st.vocab * 2,
                    "gbs": st.rows * st.vocab * 2 / (accept_us * 1e-6) / 1e9,
-                   "kernel": "q3kv_accept_greedy (argmax + acceptance kernels), bf16 logits, once per step"},
+                   "kernel": "q3kv_accept_greedy (argmax + acceptance kernels), bf16 logits, once per step",
+                   "sampled_top_p_us": nucleus_us,
+                   "sampled_top_p_kernel": "q3kv_accept_sample_nucleus (temperature 1.0, top-p 0.95): max, "
+                                           "radix select of the cut (2 levels), nucleus Gumbel-max, acceptance"},
         "clocks": clock_info,
         "gpu_launches": args.steps * Ly * st.launches_per_layer(),
         "e2e": e2e,
