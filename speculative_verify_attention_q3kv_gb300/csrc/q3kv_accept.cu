@@ -182,6 +182,50 @@ __device__ __forceinline__ float noise_uniform(uint64_t seed, uint32_t row, uint
     return ((float)(uint32_t)(z >> 41) + 0.5f) * (1.0f / 8388608.0f);
 }
 
+// f(k, logit) for every vocabulary entry k of [c0, c1) of one row, with four
+// loads of each thread in flight at once: 16-byte loads when the rows are
+// 16-byte aligned (chunk bounds are then multiples of 16 bytes too), else
+// element loads.
+template <typename T, typename F>
+__device__ __forceinline__ void for_each_logit(const AcceptArgs& a, const T* lg, int64_t c0, int64_t c1, F&& f) {
+    constexpr int kU = 4;
+    if (a.vec_ok) {
+        constexpr int kVec = 16 / sizeof(T);
+        const uint4* p = reinterpret_cast<const uint4*>(lg + c0);
+        const int64_t n = (c1 - c0) / kVec;
+        for (int64_t k0 = threadIdx.x; k0 < n; k0 += kU * kArgThreads) {
+            uint4 u[kU];
+#pragma unroll
+            for (int r = 0; r < kU; ++r) {
+                const int64_t k = k0 + (int64_t)r * kArgThreads;
+                u[r] = k < n ? __ldcs(p + k) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int r = 0; r < kU; ++r) {
+                const int64_t k = k0 + (int64_t)r * kArgThreads;
+                if (k >= n) break;
+                const T* e = reinterpret_cast<const T*>(&u[r]);
+#pragma unroll
+                for (int m = 0; m < kVec; ++m) f(c0 + k * kVec + m, to_f(e[m]));
+            }
+        }
+    } else {
+        for (int64_t k0 = c0 + threadIdx.x; k0 < c1; k0 += kU * kArgThreads) {
+            float v[kU];
+#pragma unroll
+            for (int r = 0; r < kU; ++r) {
+                const int64_t k = k0 + (int64_t)r * kArgThreads;
+                v[r] = k < c1 ? to_f(lg[k]) : 0.0f;
+            }
+#pragma unroll
+            for (int r = 0; r < kU; ++r) {
+                const int64_t k = k0 + (int64_t)r * kArgThreads;
+                if (k < c1) f(k, v[r]);
+            }
+        }
+    }
+}
+
 // Per (row, chunk): online (max, sum of exp) of logits / tau, and the best
 // Gumbel key overall and without the row's next query token.
 struct SampleStat {
@@ -235,8 +279,8 @@ __global__ void __launch_bounds__(kArgThreads) sample_stats_kernel(AcceptArgs a)
     const int excl = row + 1 < a.num_rows ? a.tokens[row + 1] : -1;
     SampleStat st = stat_empty();
     bool nan = false;
-    for (int64_t k = c0 + threadIdx.x; k < c1; k += kArgThreads) {
-        const float l = to_f(lg[k]) * a.inv_tau;
+    for_each_logit(a, lg, c0, c1, [&](int64_t k, float raw) {
+        const float l = raw * a.inv_tau;
         nan |= (l != l);
         // running max and sum of exp(l - max)
         if (l > st.m) {
@@ -248,7 +292,7 @@ __global__ void __launch_bounds__(kArgThreads) sample_stats_kernel(AcceptArgs a)
         const float key = l - logf(-logf(noise_uniform(a.seed, (uint32_t)row, (uint32_t)k)));
         if (beats(key, (int)k, st.k1, st.i1)) { st.k1 = key; st.i1 = (int)k; }
         if ((int)k != excl && beats(key, (int)k, st.k2, st.i2)) { st.k2 = key; st.i2 = (int)k; }
-    }
+    });
     st = stat_warp(st);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = st;
     if (__any_sync(0xffffffffu, nan) && (threadIdx.x & 31) == 0 && a.status)
@@ -374,7 +418,6 @@ cudaError_t launch_accept_sample(const AcceptArgs& a, cudaStream_t stream) {
 namespace q3kv {
 namespace {
 
-constexpr double kFixScale = 1099511627776.0;   // 2^40
 
 struct NucleusRow {
     float m;                       // max of l / tau
@@ -410,11 +453,11 @@ __global__ void __launch_bounds__(kArgThreads) nucleus_max_kernel(AcceptArgs a) 
     const T* lg = static_cast<const T*>(a.logits) + (int64_t)row * a.vocab;
     float m = -CUDART_INF_F;
     bool nan = false;
-    for (int64_t k = c0 + threadIdx.x; k < c1; k += kArgThreads) {
-        const float l = to_f(lg[k]) * a.inv_tau;
+    for_each_logit(a, lg, c0, c1, [&](int64_t, float raw) {
+        const float l = raw * a.inv_tau;
         nan |= (l != l);
         m = fmaxf(m, l);
-    }
+    });
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     if (__any_sync(0xffffffffu, nan) && (threadIdx.x & 31) == 0 && a.status) atomicOr(a.status, Q3KV_STATUS_NONFINITE_INPUT);
@@ -453,12 +496,16 @@ __global__ void __launch_bounds__(256) nucleus_init_kernel(AcceptArgs a) {
 }
 
 // Per (chunk, row): fixed-point mass histogram of the next 8 key bits of the
-// tokens whose higher bits equal the prefix.
+// tokens whose higher bits equal the prefix.  Each warp adds into its own
+// shared-memory histogram (logits bunch into few bins at the top levels, so a
+// shared one would serialise the warps); the eight are summed at the end.
 template <typename T>
 __global__ void __launch_bounds__(kArgThreads) nucleus_hist_kernel(AcceptArgs a, int level) {
-    __shared__ unsigned long long h[256];
+    __shared__ unsigned long long h[kArgThreads / 32][256];
     const int row = blockIdx.y, chunk = blockIdx.x;
-    h[threadIdx.x] = 0ull;
+    const int warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int w = 0; w < kArgThreads / 32; ++w) h[w][threadIdx.x] = 0ull;
     __syncthreads();
     const NucleusRow* r = nrow(a, row);
     const float m = r->m;
@@ -467,19 +514,28 @@ __global__ void __launch_bounds__(kArgThreads) nucleus_hist_kernel(AcceptArgs a,
     const int64_t c0 = (int64_t)chunk * a.chunk_elems;
     const int64_t c1 = min((int64_t)a.vocab, c0 + a.chunk_elems);
     const T* lg = static_cast<const T*>(a.logits) + (int64_t)row * a.vocab;
-    for (int64_t k = c0 + threadIdx.x; k < c1; k += kArgThreads) {
-        const float raw = to_f(lg[k]);
+    for_each_logit(a, lg, c0, c1, [&](int64_t, float raw) {
         const uint32_t key = order_key(raw);
-        if (level > 0 && (key >> (shift + 8)) != prefix) continue;
-        const unsigned long long mass = __double2ull_rn((double)__expf(raw * a.inv_tau - m) * kFixScale);
-        if (mass) atomicAdd(&h[(key >> shift) & 0xFFu], mass);
-    }
+        if (level > 0 && (key >> (shift + 8)) != prefix) return;
+        // mass = round(e 2^40) for e = e^(l/tau - max) <= 1, as an exact split
+        // at 2^20: e 2^20 and its fraction are exact floats
+        const float e20 = __expf(raw * a.inv_tau - m) * 1048576.0f;
+        const uint32_t hi = (uint32_t)e20;
+        const uint32_t lo = __float2uint_rn((e20 - (float)hi) * 1048576.0f);
+        const unsigned long long mass = ((unsigned long long)hi << 20) + lo;
+        if (mass) atomicAdd(&h[warp][(key >> shift) & 0xFFu], mass);
+    });
     __syncthreads();
-    if (h[threadIdx.x]) atomicAdd(&nhist(a, row)[threadIdx.x], h[threadIdx.x]);
+    unsigned long long t = 0ull;
+#pragma unroll
+    for (int w = 0; w < kArgThreads / 32; ++w) t += h[w][threadIdx.x];
+    if (t) atomicAdd(&nhist(a, row)[threadIdx.x], t);
 }
 
 // One CTA per row: the bin where the mass counted from the top first reaches
 // the target; extends the prefix; clears the histogram for the next level.
+// Warp 0 scans: lane l holds bins 8 (31 - l) .. 8 (31 - l) + 7 (the top bins
+// in lane 0), and a prefix sum over the lanes gives each lane the mass above.
 __global__ void __launch_bounds__(256) nucleus_select_kernel(AcceptArgs a, int level, int last) {
     const int row = blockIdx.x;
     __shared__ unsigned long long h[256];
@@ -487,29 +543,48 @@ __global__ void __launch_bounds__(256) nucleus_select_kernel(AcceptArgs a, int l
     h[threadIdx.x] = gh[threadIdx.x];
     __syncthreads();
     gh[threadIdx.x] = 0ull;
-    if (threadIdx.x != 0) return;
+    if (threadIdx.x >= 32) return;
+    const int lane = threadIdx.x;
     NucleusRow* r = nrow(a, row);
+    const int base = 8 * (31 - lane);
+    unsigned long long mine = 0ull;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mine += h[base + j];
+    unsigned long long incl = mine;                 // lanes 0..lane (lane 0 = the top bins)
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    unsigned long long target;
     if (level == 0) {
-        unsigned long long total = 0ull;
-        for (int b = 0; b < 256; ++b) total += h[b];
-        double t = ceil((double)a.top_p * (double)total);
-        r->target = t < (double)total ? (unsigned long long)t : total;
+        const unsigned long long total = __shfl_sync(0xffffffffu, incl, 31);
+        const double t = ceil((double)a.top_p * (double)total);
+        target = t < (double)total ? (unsigned long long)t : total;
+        if (lane == 0) r->target = target;
+    } else {
+        target = r->target;
     }
-    const unsigned long long target = r->target;
-    unsigned long long cum = r->above;
-    int sel = 0;
-    for (int b = 255; b >= 0; --b) {
-        if (cum + h[b] >= target) {
-            sel = b;
-            break;
+    const unsigned long long above0 = r->above;
+    // the first lane from the top whose inclusive mass reaches the target
+    const unsigned hit = __ballot_sync(0xffffffffu, above0 + incl >= target);
+    const int sl = hit ? __ffs(hit) - 1 : 31;
+    if (lane == sl) {
+        unsigned long long cum = above0 + incl - mine;     // mass above this lane's bins
+        int sel = base;
+        for (int b = base + 7; b >= base; --b) {
+            if (cum + h[b] >= target) {
+                sel = b;
+                break;
+            }
+            cum += h[b];
         }
-        cum += h[b];
-    }
-    r->prefix = (r->prefix << 8) | (uint32_t)sel;
-    r->above = cum;
-    if (last) {
-        r->key_star = r->prefix << (24 - 8 * level);   // bf16 stops after two levels: low bits of the key are the same
-        r->zn = cum + h[sel];
+        r->prefix = (r->prefix << 8) | (uint32_t)sel;
+        r->above = cum;
+        if (last) {
+            r->key_star = r->prefix << (24 - 8 * level);   // bf16 stops after two levels: the low key bits are the same
+            r->zn = cum + h[sel];
+        }
     }
 }
 
@@ -525,13 +600,12 @@ __global__ void __launch_bounds__(kArgThreads) nucleus_gumbel_kernel(AcceptArgs 
     const int excl = row + 1 < a.num_rows ? a.tokens[row + 1] : -1;
     const uint32_t key_star = nrow(a, row)->key_star | low_fill;
     SampleStat st = stat_empty();
-    for (int64_t k = c0 + threadIdx.x; k < c1; k += kArgThreads) {
-        const float raw = to_f(lg[k]);
-        if ((order_key(raw) | low_fill) < key_star) continue;
+    for_each_logit(a, lg, c0, c1, [&](int64_t k, float raw) {
+        if ((order_key(raw) | low_fill) < key_star) return;
         const float key = raw * a.inv_tau - logf(-logf(noise_uniform(a.seed, (uint32_t)row, (uint32_t)k)));
         if (beats(key, (int)k, st.k1, st.i1)) { st.k1 = key; st.i1 = (int)k; }
         if ((int)k != excl && beats(key, (int)k, st.k2, st.i2)) { st.k2 = key; st.i2 = (int)k; }
-    }
+    });
     st = stat_warp(st);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = st;
     __syncthreads();
@@ -565,8 +639,12 @@ __global__ void __launch_bounds__(32) nucleus_accept_kernel(AcceptArgs a, uint32
     if (lane + 1 < T && tok_next >= 0 && tok_next < a.vocab) {
         const NucleusRow* r = nrow(a, r0 + lane);
         const float raw = to_f(static_cast<const TIn*>(a.logits)[(int64_t)(r0 + lane) * a.vocab + tok_next]);
-        if ((order_key(raw) | low_fill) >= (r->key_star | low_fill))
-            p = (float)((double)__expf(raw * a.inv_tau - r->m) * kFixScale / (double)r->zn);
+        if ((order_key(raw) | low_fill) >= (r->key_star | low_fill)) {
+            const float e20 = __expf(raw * a.inv_tau - r->m) * 1048576.0f;   // the histogram's fixed point
+            const uint32_t hi = (uint32_t)e20;
+            const uint32_t lo = __float2uint_rn((e20 - (float)hi) * 1048576.0f);
+            p = (float)((double)(((unsigned long long)hi << 20) + lo) / (double)r->zn);
+        }
     }
     const SampleStat* pp = reinterpret_cast<const SampleStat*>(a.partial) + (int64_t)r0 * a.num_chunks;
     SampleStat mine = stat_empty();

@@ -440,7 +440,7 @@ int q3kv_accept_sample(void* stream, const void* logits, int32_t dtype, int32_t 
     a.vocab = vocab;
     a.chunk_elems = chunk;
     a.num_chunks = nch;
-    a.vec_ok = 0;
+    a.vec_ok = (aligned16(logits) && ((size_t)vocab * (dtype == Q3KV_F32 ? 4 : 2)) % 16 == 0) ? 1 : 0;
     a.q_offsets = d_q_offsets;
     a.n_q = d_n_q;
     a.tokens = d_tokens;
@@ -492,7 +492,7 @@ int q3kv_accept_sample_nucleus(void* stream, const void* logits, int32_t dtype, 
     a.vocab = vocab;
     a.chunk_elems = chunk;
     a.num_chunks = nch;
-    a.vec_ok = 0;
+    a.vec_ok = (aligned16(logits) && ((size_t)vocab * (dtype == Q3KV_F32 ? 4 : 2)) % 16 == 0) ? 1 : 0;
     a.q_offsets = d_q_offsets;
     a.n_q = d_n_q;
     a.tokens = d_tokens;
