@@ -3,7 +3,8 @@
 // Source: "Quasar" (q27 wiki) -- "Self-speculation as the whole design" (all
 // drafted tokens checked in one shared-KV MMA verify), the Defaults paragraph
 // of "Serving" (MMA verify legs: e4m3 tiles or fp16 tiles "h16", beside the fd2
-// reference), and "KV cache" (verify reads the WHT-rotated 3-bit cache).  The
+// reference), and "KV cache" (verify reads the WHT-rotated 3-bit cache; the
+// server's default fp8 E4M3 cache is the second format this kernel reads).  The
 // pages' legs are mma.sync kernels for consumer GPUs without tcgen05; this is
 // a new design for sm_103a.  The e4m3 staging of the pages is not used: it
 // adds error on top of the codec's, and the output tolerance here is tight.
@@ -20,6 +21,10 @@
 //   V_hat likewise; Q = Q_hi + Q_lo and P = P_hi + P_lo (round-to-nearest
 //   splits); each contraction sums the three leading products
 //   (hi.hi + hi.lo + lo.hi) with fp32 accumulation in TMEM.
+// The fp8 format (template FMT = kFmtFp8) decodes K and V exactly into single
+// fp16 values (one conversion per pair), so each contraction has two products
+// (K.Q_hi + K.Q_lo, V.P_hi + V.P_lo); it is not rotated, so the query kernel
+// skips H and the epilogue and merge skip H^-1.
 //
 // Contractions (M = 128 for both):
 //   S^T[p][r] = K_hat[p][:] . Q[r][:]    A = K_hat in TMEM (lane = position),
@@ -37,11 +42,11 @@
 // O^T.  Every MMA sequence is fully unrolled, its descriptors formed by
 // constant offsets.
 //
-// Records reach shared memory by bulk copies (cp.async.bulk, completing on an
-// mbarrier): one 14,336-byte copy per tile for K and one for V (a tile's 128
-// positions are contiguous in a page), two stages each, issued a tile ahead by
-// one thread of the warps that read them.  No warp waits on a global load in
-// the loop, and the dequantising warps hold no prefetch registers.
+// Records: each K thread loads its own position's record straight from the
+// pool into registers a tile (fp8: half a record) ahead; the V warps each
+// bulk-copy their two 16-record groups of a tile into shared memory
+// (cp.async.bulk completing on their own mbarrier) and refill them as soon as
+// they have read them.  A tile's 128 positions are contiguous in a page.
 //
 // Warp roles (16 warps), handing tiles on with mbarriers:
 //   A   warps 0-3   softmax: thread = position; reads S from TMEM;
@@ -51,19 +56,20 @@
 //                   cross-lane maximum; P = 2^(s - m) <= 256 goes to shared
 //                   memory as fp16 hi/lo; row sums accumulate per lane in TMEM
 //                   and are reduced across lanes once, after the last tile.
-//   B1  warps 4-7   thread = position: its K record from shared memory, K_hat
-//                   into TMEM in two halves (dims 0..127, 128..255), each as
-//                   soon as the QK half of the previous tile has read it.
-//   B2  warps 8-11  V_hat in 16-position sub-tiles through four shared-memory
-//                   buffers; lane = (position, 32-dim block), all four warps on
-//                   every sub-tile.
+//   B1  warps 4-7   thread = position: its K record in registers, K_hat into
+//                   TMEM in two halves (dims 0..127, 128..255), each as soon
+//                   as the QK half of the previous tile has read it.
+//   B2  warps 8-11  V_hat in 16-position sub-tiles through a ring of five
+//                   shared-memory buffers; warp q fills sub-tiles q and q + 4
+//                   of each tile, lane = (position, 32-dim block).
 //   MQa, MQb  warps 12-13   one thread each issues a QK half
 //   MP0, MP1  warps 14-15   one thread each issues the PV of an O^T half
 // TMEM (512 columns): K_hat hi | K_hat lo | S | row-sum partials | O^T dims 0..127 | 128..255.
 //
-// After the last tile the A warps read O^T (thread = two output dims) and
-// either finish the rows (one split: divide by l, rotate back by H) or store
-// the split partial (m, l, o) for the merge kernel.
+// After the last tile the A warps read O^T (thread = one output dim, 32 rows
+// per TMEM round trip) and either finish the rows (one split: times 1/l, then
+// H back for the rotated format) or store the split partial (m, l, o) for the
+// merge kernel.
 //
 // Every mbarrier wait is bounded (about a second); on a timeout the CTA sets
 // Q3KV_STATUS_TIMEOUT, stops issuing, waits (bounded) for the MMAs and copies
