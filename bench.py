@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--split", type=int, default=0, help="positions per split (0 = library policy)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill", type=int, default=0,
+                    help="instead of the verify step: a fresh prefill of this many tokens (append + prefill "
+                         "attention over the 3-bit cache, every layer of the workload, one slot)")
     ap.add_argument("--kv", default="q3", choices=["q3", "fp8"],
                     help="cache format: the 3-bit rotated codec, or the fp8 E4M3 comparison format")
     return ap.parse_args()
@@ -537,10 +540,98 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill(args, rank, world, local, pg):
+    """A fresh prefill of args.prefill tokens per layer: quantise-append, then causal attention."""
+    import torch
+
+    from speculative_verify_attention_q3kv_gb300 import api
+    from speculative_verify_attention_q3kv_gb300 import build as b
+
+    b.build()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    w = qi.WORKLOADS[args.workload]
+    T, Ly, H, Hq = args.prefill, w.num_layers, w.num_kv_heads, w.num_q_heads
+    pages = (T + 255) // 256
+    desc = api.make_desc(Ly, H, pages)
+    pool = torch.zeros(api.pool_bytes(desc), dtype=torch.uint8, device=device)
+    i32 = dict(dtype=torch.int32, device=device)
+    pt = torch.arange(pages, **i32)[None]
+    zero, n_new, offs, ctx = (torch.tensor([0], **i32), torch.tensor([T], **i32), torch.tensor([0, T], **i32),
+                              torch.tensor([T], **i32))
+    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    g = torch.Generator(device=device)
+    g.manual_seed(2000 + w.seed)
+    k = torch.empty((Ly, T, H, 256), dtype=dt, device=device)
+    v = torch.empty_like(k)
+    for l in range(Ly):
+        for h in range(H):
+            qi.torch_fill_kv_(k[l, :, h], w, l, h, 0, g)
+            qi.torch_fill_kv_(v[l, :, h], w, l, h, 1, g)
+    q = torch.randn((Ly, T, Hq, 256), generator=g, device=device).to(dt)
+    out = torch.empty((Ly, T, Hq, 256), dtype=torch.float32, device=device)
+    impl = {"auto": 0, "fma": 1, "mma": 2}[args.verify_impl]
+    ws = torch.zeros(max(api.prefill_workspace_bytes(desc, 1, T, T, impl, args.split), 16), dtype=torch.uint8,
+                     device=device)
+    status = torch.zeros(1, **i32)
+
+    def step(append=True):
+        for l in range(Ly):
+            if append:
+                api.append(desc, pool, pt, zero, n_new, offs, T, l, k[l], v[l], status)
+            api.prefill_attn(desc, pool, pt, ctx, n_new, offs, T, T, l, q[l], out[l], ws, impl, args.split, status)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    aev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(pg)
+    torch.cuda.synchronize()
+    clocks.start()
+    for s_ in range(args.steps):
+        flush.zero_()
+        ev[s_][0].record()
+        step()
+        ev[s_][1].record()
+    for s_ in range(args.steps):
+        flush.zero_()
+        aev[s_][0].record()
+        step(append=False)
+        aev[s_][1].record()
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    barrier(pg)
+    assert int(status.item()) == 0, "device status flagged during the prefill benchmark"
+    total_s = max_over_ranks(pg, sum(a.elapsed_time(b_) for a, b_ in ev) / 1e3)
+    attn_s = sum(a.elapsed_time(b_) for a, b_ in aev) / 1e3
+    if rank != 0:
+        return
+    # causal rows: token t reads t + 1 positions of 224 bytes per kv head
+    attended = H * T * (T + 1) // 2
+    line = {"metric": "prefill tokens/s (append + causal prefill attention over the 3-bit cache, all layers)",
+            "value": world * T * args.steps / total_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": total_s * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+            "data": "synthetic (seeded, the workload's K/V distributions)",
+            "config": {"workload": f"prefill{T}_{Ly}layer", "layers": Ly, "kv_heads": H, "q_heads": Hq,
+                       "new_tokens": T, "context_before": 0, "verify_impl": args.verify_impl,
+                       "l2": "flushed between timed steps (256 MiB write)", "launch": "stream (no graph)"},
+            "attention_us_per_layer": attn_s * 1e6 / (args.steps * Ly),
+            "attention_only_tokens_per_s": T * args.steps / attn_s,
+            "attended_kv_bytes_per_layer": attended * 224,
+            "clocks": clock_info, "e2e": None, "cpu_baseline": None}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local, pg = dist_init(args.gpus)
-    if args.impl == "reference":
+    if args.prefill and args.impl != "reference":
+        run_prefill(args, rank, world, local, pg)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local, pg)

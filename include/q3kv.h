@@ -215,6 +215,27 @@ Q3KV_API int q3kv_verify_attn_noalloc(void* stream, const q3kv_cache_desc* desc,
                      const void* q, int32_t dtype, float* out,
                      int32_t impl, int32_t split_positions, int32_t* d_status);
 
+/* ---- prefill attention over the 3-bit cache --------------------------------------
+ * Source: the "turbo3 3-bit KV cache" bullet of the "Quasar" (q27) wiki (the
+ * cache serves decode, verify and batched prefill) and the prefill follow-ons
+ * bullet (a prefill-attention kernel).  A prefill is the verify step with many
+ * new tokens: append them with q3kv_append, then q3kv_prefill_attn computes
+ * the same causal attention as q3kv_verify_attn (new token t of slot b sees
+ * positions [0, ctx_len - n_new + t]) for up to 8192 new tokens per slot.
+ * Arguments, layout, workspace contract, errors and status bits are those of
+ * q3kv_verify_attn, with d_n_new / max_n_new in place of d_n_q / max_n_q and
+ * the workspace sized by q3kv_prefill_workspace_bytes.  Each CTA of the
+ * tensor-core leg reads only the positions its rows can see. */
+Q3KV_API int q3kv_prefill_workspace_bytes(const q3kv_cache_desc* desc, int32_t num_slots, int64_t max_ctx_len,
+                         int32_t max_n_new, int32_t impl, int32_t split_positions, size_t* bytes);
+Q3KV_API int q3kv_prefill_attn(void* stream, const q3kv_cache_desc* desc, const void* d_pool,
+                     const int32_t* d_page_table, int32_t max_pages_per_slot,
+                     const int32_t* d_ctx_len, const int32_t* d_n_new, const int32_t* d_q_offsets,
+                     int32_t num_slots, int64_t max_ctx_len, int32_t max_n_new, int32_t layer,
+                     const void* q, int32_t dtype, float* out,
+                     int32_t impl, int32_t split_positions,
+                     void* d_workspace, size_t workspace_bytes, int32_t* d_status);
+
 /* ---- fp8 E4M3 comparison cache ------------------------------------------------
  * The format the pages' server uses by default ("KV cache" stack bullet of the
  * "Quasar" (q27) wiki): K and V stored as fp8 E4M3 with a scale-free,

@@ -68,6 +68,11 @@ PROTOTYPES = {
     "q3kv_verify_attn_noalloc": (c_int32, [c_void_p, P_desc, c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
                                            c_void_p, c_int32, c_int64, c_int32, c_int32, c_void_p, c_int32,
                                            c_void_p, c_int32, c_int32, c_void_p]),
+    "q3kv_prefill_workspace_bytes": (c_int32, [P_desc, c_int32, c_int64, c_int32, c_int32, c_int32,
+                                               ctypes.POINTER(c_size_t)]),
+    "q3kv_prefill_attn": (c_int32, [c_void_p, P_desc, c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_void_p,
+                                    c_int32, c_int64, c_int32, c_int32, c_void_p, c_int32, c_void_p,
+                                    c_int32, c_int32, c_void_p, c_size_t, c_void_p]),
     "q3kv_fp8_pool_bytes": (c_int32, [P_desc, ctypes.POINTER(c_size_t)]),
     "q3kv_fp8_append": (c_int32, [c_void_p, P_desc, c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_void_p,
                                   c_int32, c_int32, c_int32, c_void_p, c_void_p, c_int32, c_void_p]),

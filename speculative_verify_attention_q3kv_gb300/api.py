@@ -146,6 +146,30 @@ def verify_attn_noalloc(desc: CacheDesc, pool: torch.Tensor, page_table: torch.T
     check(rc, "q3kv_verify_attn_noalloc")
 
 
+def prefill_workspace_bytes(desc: CacheDesc, num_slots: int, max_ctx_len: int, max_n_new: int,
+                            impl: int = _lib.Q3KV_IMPL_AUTO, split_positions: int = 0) -> int:
+    n = ctypes.c_size_t()
+    check(_lib.load().q3kv_prefill_workspace_bytes(ctypes.byref(desc), num_slots, max_ctx_len, max_n_new, impl,
+                                                   split_positions, ctypes.byref(n)), "q3kv_prefill_workspace_bytes")
+    return n.value
+
+
+def prefill_attn(desc: CacheDesc, pool: torch.Tensor, page_table: torch.Tensor, ctx_len: torch.Tensor,
+                 n_new: torch.Tensor, q_offsets: torch.Tensor, max_ctx_len: int, max_n_new: int, layer: int,
+                 q: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
+                 impl: int = _lib.Q3KV_IMPL_AUTO, split_positions: int = 0,
+                 status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """q3kv_prefill_attn: causal attention of up to 8192 appended tokens per slot over the 3-bit cache."""
+    if out.dtype != torch.float32:
+        raise TypeError("out must be float32")
+    rc = _lib.load().q3kv_prefill_attn(_stream(stream), ctypes.byref(desc), _ptr(pool), _ptr(page_table),
+                                       page_table.shape[1], _ptr(ctx_len), _ptr(n_new), _ptr(q_offsets),
+                                       ctx_len.shape[0], max_ctx_len, max_n_new, layer, _ptr(q), _dtype_code(q),
+                                       _ptr(out), impl, split_positions, _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _ptr(status))
+    check(rc, "q3kv_prefill_attn")
+
+
 def fp8_pool_bytes(desc: CacheDesc) -> int:
     """q3kv_fp8_pool_bytes: bytes of an fp8 E4M3 comparison pool (256-byte records)."""
     n = ctypes.c_size_t()

@@ -58,8 +58,8 @@ struct Plan {
 // Split-K policy: enough (slot, kv head, row chunk, split) CTAs to cover the
 // GPU about twice over, splits a whole number of pages.
 int make_plan(const q3kv_cache_desc* d, int32_t num_slots, int64_t max_ctx, int32_t max_n_q, int32_t impl,
-              int32_t split_positions, Plan* p) {
-    if (num_slots < 0 || max_ctx < 0 || max_n_q < 0 || max_n_q > kMaxNq) return Q3KV_ERR_INVALID_ARG;
+              int32_t split_positions, Plan* p, int32_t max_tokens = kMaxNq) {
+    if (num_slots < 0 || max_ctx < 0 || max_n_q < 0 || max_n_q > max_tokens) return Q3KV_ERR_INVALID_ARG;
     if (split_positions < 0 || split_positions % kPageSize != 0) return Q3KV_ERR_INVALID_ARG;
     if (max_ctx > (int64_t)INT32_MAX - kPageSize) return Q3KV_ERR_INVALID_ARG;
     if (impl == Q3KV_IMPL_AUTO) impl = Q3KV_IMPL_MMA;
@@ -223,20 +223,22 @@ int verify_impl(int fmt, void* stream, const q3kv_cache_desc* desc, const void* 
                 int32_t max_pages_per_slot, const int32_t* d_ctx_len, const int32_t* d_n_q,
                 const int32_t* d_q_offsets, int32_t num_slots, int64_t max_ctx_len, int32_t max_n_q,
                 int32_t layer, const void* q, int32_t dtype, float* out, int32_t impl,
-                int32_t split_positions, void* d_workspace, size_t workspace_bytes, int32_t* d_status) {
+                int32_t split_positions, void* d_workspace, size_t workspace_bytes, int32_t* d_status,
+                int32_t max_tokens = kMaxNq) {
     int e = check_desc(desc);
     if (e != Q3KV_OK) return e;
     if (num_slots < 0 || max_pages_per_slot <= 0 || layer < 0 || layer >= desc->num_layers)
         return Q3KV_ERR_INVALID_ARG;
     if (num_slots > 65535) return Q3KV_ERR_UNSUPPORTED;
     if (dtype != Q3KV_F32 && dtype != Q3KV_BF16) return Q3KV_ERR_INVALID_ARG;
-    if (max_n_q > kMaxNq) return Q3KV_ERR_UNSUPPORTED;
+    if (max_n_q > max_tokens) return Q3KV_ERR_UNSUPPORTED;
     if (impl < Q3KV_IMPL_AUTO || impl > Q3KV_IMPL_MMA) return Q3KV_ERR_INVALID_ARG;
     if (fmt == kFmtFp8 && impl == Q3KV_IMPL_FMA) return Q3KV_ERR_UNSUPPORTED;   // tensor-core leg only
     Plan p;
-    e = make_plan(desc, num_slots, max_ctx_len, max_n_q, impl, split_positions, &p);
+    e = make_plan(desc, num_slots, max_ctx_len, max_n_q, impl, split_positions, &p, max_tokens);
     if (e != Q3KV_OK) return e;
     if (num_slots == 0 || max_n_q == 0 || max_ctx_len == 0) return Q3KV_OK;
+    if ((int64_t)desc->num_kv_heads * p.row_chunks > 65535) return Q3KV_ERR_UNSUPPORTED;   // grid.y
     if (!d_pool || !d_page_table || !d_ctx_len || !d_n_q || !d_q_offsets || !q || !out) return Q3KV_ERR_INVALID_ARG;
     if (!aligned16(d_pool) || !aligned16(q) || !aligned16(out)) return Q3KV_ERR_INVALID_ARG;
     if (workspace_bytes < p.total() || (p.total() > 0 && !d_workspace)) return Q3KV_ERR_WORKSPACE_TOO_SMALL;
@@ -336,6 +338,28 @@ int q3kv_fp8_verify_attn(void* stream, const q3kv_cache_desc* desc, const void* 
     return verify_impl(kFmtFp8, stream, desc, d_pool, d_page_table, max_pages_per_slot, d_ctx_len, d_n_q,
                        d_q_offsets, num_slots, max_ctx_len, max_n_q, layer, q, dtype, out, impl, split_positions,
                        d_workspace, workspace_bytes, d_status);
+}
+
+int q3kv_prefill_workspace_bytes(const q3kv_cache_desc* desc, int32_t num_slots, int64_t max_ctx_len,
+                                 int32_t max_n_new, int32_t impl, int32_t split_positions, size_t* bytes) {
+    int e = check_desc(desc);
+    if (e != Q3KV_OK) return e;
+    if (!bytes) return Q3KV_ERR_INVALID_ARG;
+    Plan p;
+    e = make_plan(desc, num_slots, max_ctx_len, max_n_new, impl, split_positions, &p, kMaxPrefillNq);
+    if (e != Q3KV_OK) return e;
+    *bytes = p.total();
+    return Q3KV_OK;
+}
+
+int q3kv_prefill_attn(void* stream, const q3kv_cache_desc* desc, const void* d_pool, const int32_t* d_page_table,
+                      int32_t max_pages_per_slot, const int32_t* d_ctx_len, const int32_t* d_n_new,
+                      const int32_t* d_q_offsets, int32_t num_slots, int64_t max_ctx_len, int32_t max_n_new,
+                      int32_t layer, const void* q, int32_t dtype, float* out, int32_t impl,
+                      int32_t split_positions, void* d_workspace, size_t workspace_bytes, int32_t* d_status) {
+    return verify_impl(kFmtQ3, stream, desc, d_pool, d_page_table, max_pages_per_slot, d_ctx_len, d_n_new,
+                       d_q_offsets, num_slots, max_ctx_len, max_n_new, layer, q, dtype, out, impl, split_positions,
+                       d_workspace, workspace_bytes, d_status, kMaxPrefillNq);
 }
 
 }  // extern "C"

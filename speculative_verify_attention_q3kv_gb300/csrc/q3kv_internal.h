@@ -15,6 +15,7 @@ constexpr int kGroup = 8;            // q heads per kv head
 constexpr int kRecordBytes = 112;    // one coded vector
 constexpr int kCodeWords = 24;       // 96 bytes of codes
 constexpr int kMaxNq = 16;           // query tokens per slot and step
+constexpr int kMaxPrefillNq = 8192;  // new tokens per slot of one prefill call
 constexpr int kMaxRows = kGroup * kMaxNq;
 
 constexpr int kFp8RecordBytes = 256;  // fp8 E4M3 comparison format: one byte per element

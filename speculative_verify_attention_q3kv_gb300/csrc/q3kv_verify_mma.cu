@@ -603,9 +603,13 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
     }
     if (split >= n_splits) return;
     const int p_begin = split * a.split_pages * kPageSize;
-    const int p_end = min(L, p_begin + a.split_pages * kPageSize);
-    const int n_tiles = (p_end - p_begin + kTileP - 1) / kTileP;
     const int Nctx = L - T;
+    // positions past the causal limit of this CTA's last row are masked for all
+    // of its rows, so they are not read (long prefills: later rows see more);
+    // at least one position is kept so every CTA of a split writes its partial
+    const int p_vis = Nctx + (row0 + Rc - 1) / kGroup + 1;
+    const int p_end = min(min(L, p_begin + a.split_pages * kPageSize), max(p_vis, p_begin + 1));
+    const int n_tiles = (p_end - p_begin + kTileP - 1) / kTileP;
     const int Hq = a.num_kv_heads * kGroup;
     const int64_t q_base = a.q_offsets[slot];
     const int N = (Rc + 15) & ~15;      // MMA N: rows padded to 16
