@@ -1,0 +1,61 @@
+"""Multi-process path of the benchmark on CPU (world size 2, gloo).
+
+The verify path shards as independent replicas (one per GPU, no collective on
+the data path); the only cross-rank steps are the barrier around the timed
+region and the max over ranks of the timed seconds.  These tests run those
+helpers, and the reference arm under torchrun, as two CPU processes.
+"""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out_dir):
+    os.environ.update({"RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    sys.path.insert(0, ROOT)
+    import bench
+
+    r, wsz, local, pg = bench.dist_init(world)
+    bench.barrier(pg)
+    m = bench.max_over_ranks(pg, 1.5 + rank)          # rank-dependent timed seconds
+    bench.barrier(pg)
+    with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as f:
+        json.dump({"rank": r, "world": wsz, "local": local, "max": m}, f)
+    pg.destroy_process_group()
+
+
+def test_barrier_and_max_over_two_ranks(tmp_path):
+    import torch.multiprocessing as mp
+
+    port = _free_port()
+    mp.start_processes(_worker, args=(2, port, str(tmp_path)), nprocs=2, start_method="spawn", join=True)
+    got = [json.load(open(tmp_path / f"rank{r}.json")) for r in range(2)]
+    assert [g["rank"] for g in got] == [0, 1] and all(g["world"] == 2 for g in got)
+    assert all(g["max"] == 2.5 for g in got)           # every rank sees the slowest rank's time
+
+
+def test_reference_arm_under_torchrun_prints_one_line():
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference",
+           "--gpus", "2", "--workload", "1", "--steps", "1", "--warmup", "3"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1                              # rank 0 alone prints
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle"
