@@ -11,7 +11,9 @@ A plain, slow, obviously correct restatement of what the hot path computes:
 * ``accept``    -- greedy acceptance of a verify step's drafts and the commit
                    (rollback) of the cache length;
 * ``fp8``       -- the fp8 E4M3 comparison format (saturating, unscaled,
-                   unrotated), its paged cache and plain-basis attention.
+                   unrotated), its paged cache and plain-basis attention;
+* ``turbo5k``   -- the turbo5k-style cache: 5-bit Lloyd-Max K (root-mean-square
+                   scale per 128 dims) with the 3-bit V, its paged cache.
 
 Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
 may import this package.  The product path (the CUDA library and its Python
