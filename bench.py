@@ -58,8 +58,9 @@ def parse():
     ap.add_argument("--prefill", type=int, default=0,
                     help="instead of the verify step: a fresh prefill of this many tokens (append + prefill "
                          "attention over the 3-bit cache, every layer of the workload, one slot)")
-    ap.add_argument("--kv", default="q3", choices=["q3", "fp8"],
-                    help="cache format: the 3-bit rotated codec, or the fp8 E4M3 comparison format")
+    ap.add_argument("--kv", default="q3", choices=["q3", "fp8", "t5k"],
+                    help="cache format: the 3-bit rotated codec, the fp8 E4M3 comparison format, or the "
+                         "turbo5k-style 5-bit K / 3-bit V format (CUDA-core leg)")
     return ap.parse_args()
 
 
@@ -180,10 +181,11 @@ class Step:
         self.num_pages = sum(pages)
         self.desc = api.make_desc(w.num_layers, w.num_kv_heads, self.num_pages)
         self.fp8 = kv == "fp8"
-        self.record_bytes = 256 if self.fp8 else 112
-        self._append = api.fp8_append if self.fp8 else api.append
-        self._verify = api.fp8_verify_attn if self.fp8 else api.verify_attn
-        pool_bytes = api.fp8_pool_bytes(self.desc) if self.fp8 else api.pool_bytes(self.desc)
+        # bytes per position and kv head, K and V together
+        self.position_bytes = {"q3": 224, "fp8": 512, "t5k": 164 + 112}[kv]
+        self._append = {"q3": api.append, "fp8": api.fp8_append, "t5k": api.t5k_append}[kv]
+        self._verify = {"q3": api.verify_attn, "fp8": api.fp8_verify_attn, "t5k": api.t5k_verify_attn}[kv]
+        pool_bytes = {"q3": api.pool_bytes, "fp8": api.fp8_pool_bytes, "t5k": api.t5k_pool_bytes}[kv](self.desc)
         self.pool = torch.zeros(pool_bytes, dtype=torch.uint8, device=device)
         pt = np.full((self.S, max(pages)), -1, np.int32)
         k = 0
@@ -202,6 +204,8 @@ class Step:
         self.max_ctx = max(self.Ltot)
         self.dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
         self.impl = {"auto": 0, "fma": 1, "mma": 2}[verify_impl]
+        if kv == "t5k":
+            self.impl = 1                      # the turbo5k-style cache is read by the CUDA-core leg
         self.split = split
         self.ws = torch.zeros(api.workspace_bytes(self.desc, self.S, self.max_ctx, self.max_new, self.impl, split),
                               dtype=torch.uint8, device=device)
@@ -256,7 +260,7 @@ class Step:
         assert int(self.status.item()) == 0, "prefill flagged a device status"
 
     def kv_bytes_per_layer(self):
-        return sum(self.Ltot) * self.w.num_kv_heads * 2 * self.record_bytes
+        return sum(self.Ltot) * self.w.num_kv_heads * self.position_bytes
 
     def run(self, append=True, verify=True):
         """One step: for every layer, append the new K/V then verify the new tokens."""
@@ -425,9 +429,10 @@ def run_ours(args, rank, world, local, pg):
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded; K,V per-channel 10^U(0,1) outliers, Q N(0,1))" if w.kv_dist == "loguniform10"
                 else "synthetic (seeded; K,V N(0,1) with 4 outlier channels x8)",
-        "config": {"workload": w.name if args.kv == "q3" else w.name + "_fp8kv",
-                   "kv_format": "q3kv 3-bit WHT, 112 B per head vector" if args.kv == "q3"
-                   else "fp8 e4m3, 256 B per head vector",
+        "config": {"workload": w.name if args.kv == "q3" else w.name + "_" + args.kv + "kv",
+                   "kv_format": {"q3": "q3kv 3-bit WHT, 112 B per head vector",
+                                 "fp8": "fp8 e4m3, 256 B per head vector",
+                                 "t5k": "turbo5k-style: 5-bit Lloyd-Max K 164 B + 3-bit V 112 B"}[args.kv],
                    "slots": w.num_slots, "layers": Ly, "kv_heads": w.num_kv_heads,
                    "q_heads": w.num_q_heads, "head_dim": w.head_dim, "ctx": st.ctx, "query_tokens": st.n_new,
                    "page_size": 256, "verify_impl": args.verify_impl, "split_positions": args.split,

@@ -266,6 +266,42 @@ Q3KV_API int q3kv_fp8_verify_attn(void* stream, const q3kv_cache_desc* desc, con
                      int32_t impl, int32_t split_positions,
                      void* d_workspace, size_t workspace_bytes, int32_t* d_status);
 
+/* ---- turbo5k-style cache: 5-bit Lloyd-Max K, 3-bit V ----------------------------
+ * Source: the turbo5k bullet of the "Quasar" (q27) wiki's stack list: 5-bit K
+ * with 32 Lloyd-Max centroids over the same WHT rotation, 82-byte K blocks per
+ * 128 dims, and the 3-bit V -- the pages' fix for the 3-bit cache's tail
+ * errors.  This library's reading:
+ *   - K: y = H x (the 3-bit codec's rotation); per 128-dim half an fp16 scale
+ *     s = root mean square of y (float32 squares summed within each run of 8
+ *     elements from its first, then over runs pairwise); v = y / s (IEEE
+ *     float32), code = the number of the 31 float32 midpoints of the float32
+ *     Lloyd-Max centroids of N(0, 1) below v (s == 0: code 16); value c_code s.
+ *   - K record, 164 bytes: bytes 0..127 the low nibbles of the 256 codes (two
+ *     per byte, even element low), 128..159 their 5th bits (element d at bit
+ *     d % 8 of byte 128 + d / 8), 160..163 the two fp16 scales.
+ *   - V record: the 3-bit codec's 112 bytes.
+ *   - Pool: per (page, layer, kv head) 256 K records then 256 V records:
+ *     ((page * L + layer) * H + head) * 70,656 + row * 164 (K), or
+ *     + 41,984 + row * 112 (V).  Pages, page tables, lengths, allocator as the
+ *     3-bit cache.
+ *   - Verify: the CUDA-core leg (impl AUTO or FMA; MMA returns
+ *     Q3KV_ERR_UNSUPPORTED); the workspace is q3kv_workspace_bytes(...) with
+ *     impl Q3KV_IMPL_FMA.
+ * Arguments, ownership, errors and status bits as q3kv_pool_bytes,
+ * q3kv_append and q3kv_verify_attn. */
+Q3KV_API int q3kv_t5k_pool_bytes(const q3kv_cache_desc* desc, size_t* bytes);
+Q3KV_API int q3kv_t5k_append(void* stream, const q3kv_cache_desc* desc, void* d_pool, const int32_t* d_page_table,
+                    int32_t max_pages_per_slot, const int32_t* d_slot_len, const int32_t* d_n_new,
+                    const int32_t* d_row_offsets, int32_t num_slots, int32_t max_n_new, int32_t layer,
+                    const void* k, const void* v, int32_t dtype, int32_t* d_status);
+Q3KV_API int q3kv_t5k_verify_attn(void* stream, const q3kv_cache_desc* desc, const void* d_pool,
+                     const int32_t* d_page_table, int32_t max_pages_per_slot,
+                     const int32_t* d_ctx_len, const int32_t* d_n_q, const int32_t* d_q_offsets,
+                     int32_t num_slots, int64_t max_ctx_len, int32_t max_n_q, int32_t layer,
+                     const void* q, int32_t dtype, float* out,
+                     int32_t impl, int32_t split_positions,
+                     void* d_workspace, size_t workspace_bytes, int32_t* d_status);
+
 /* ---- greedy acceptance and commit ------------------------------------------
  * Source: "Quasar" (q27) wiki -- the sampler paragraph of "Serving" and the
  * "Model tool protocol" bullet (greedy speculative decode is the default), and

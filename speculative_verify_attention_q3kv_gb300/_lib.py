@@ -73,6 +73,12 @@ PROTOTYPES = {
     "q3kv_prefill_attn": (c_int32, [c_void_p, P_desc, c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_void_p,
                                     c_int32, c_int64, c_int32, c_int32, c_void_p, c_int32, c_void_p,
                                     c_int32, c_int32, c_void_p, c_size_t, c_void_p]),
+    "q3kv_t5k_pool_bytes": (c_int32, [P_desc, ctypes.POINTER(c_size_t)]),
+    "q3kv_t5k_append": (c_int32, [c_void_p, P_desc, c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_void_p,
+                                  c_int32, c_int32, c_int32, c_void_p, c_void_p, c_int32, c_void_p]),
+    "q3kv_t5k_verify_attn": (c_int32, [c_void_p, P_desc, c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
+                                       c_void_p, c_int32, c_int64, c_int32, c_int32, c_void_p, c_int32, c_void_p,
+                                       c_int32, c_int32, c_void_p, c_size_t, c_void_p]),
     "q3kv_fp8_pool_bytes": (c_int32, [P_desc, ctypes.POINTER(c_size_t)]),
     "q3kv_fp8_append": (c_int32, [c_void_p, P_desc, c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_void_p,
                                   c_int32, c_int32, c_int32, c_void_p, c_void_p, c_int32, c_void_p]),

@@ -170,6 +170,42 @@ def prefill_attn(desc: CacheDesc, pool: torch.Tensor, page_table: torch.Tensor, 
     check(rc, "q3kv_prefill_attn")
 
 
+def t5k_pool_bytes(desc: CacheDesc) -> int:
+    """q3kv_t5k_pool_bytes: bytes of a turbo5k-style pool (164-byte K, 112-byte V records)."""
+    n = ctypes.c_size_t()
+    check(_lib.load().q3kv_t5k_pool_bytes(ctypes.byref(desc), ctypes.byref(n)), "q3kv_t5k_pool_bytes")
+    return n.value
+
+
+def t5k_append(desc: CacheDesc, pool: torch.Tensor, page_table: torch.Tensor, slot_len: torch.Tensor,
+               n_new: torch.Tensor, row_offsets: torch.Tensor, max_n_new: int, layer: int,
+               k: torch.Tensor, v: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """q3kv_t5k_append: 5-bit Lloyd-Max K and 3-bit V records for k, v [rows, kv_heads, 256]."""
+    if k.dtype != v.dtype:
+        raise TypeError("k and v must share a dtype")
+    rc = _lib.load().q3kv_t5k_append(_stream(stream), ctypes.byref(desc), _ptr(pool), _ptr(page_table),
+                                     page_table.shape[1], _ptr(slot_len), _ptr(n_new), _ptr(row_offsets),
+                                     slot_len.shape[0], max_n_new, layer, _ptr(k), _ptr(v), _dtype_code(k),
+                                     _ptr(status))
+    check(rc, "q3kv_t5k_append")
+
+
+def t5k_verify_attn(desc: CacheDesc, pool: torch.Tensor, page_table: torch.Tensor, ctx_len: torch.Tensor,
+                    n_q: torch.Tensor, q_offsets: torch.Tensor, max_ctx_len: int, max_n_q: int, layer: int,
+                    q: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
+                    impl: int = _lib.Q3KV_IMPL_FMA, split_positions: int = 0,
+                    status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """q3kv_t5k_verify_attn: verify attention over the turbo5k-style cache (CUDA-core leg)."""
+    if out.dtype != torch.float32:
+        raise TypeError("out must be float32")
+    rc = _lib.load().q3kv_t5k_verify_attn(_stream(stream), ctypes.byref(desc), _ptr(pool), _ptr(page_table),
+                                          page_table.shape[1], _ptr(ctx_len), _ptr(n_q), _ptr(q_offsets),
+                                          ctx_len.shape[0], max_ctx_len, max_n_q, layer, _ptr(q), _dtype_code(q),
+                                          _ptr(out), impl, split_positions, _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _ptr(status))
+    check(rc, "q3kv_t5k_verify_attn")
+
+
 def fp8_pool_bytes(desc: CacheDesc) -> int:
     """q3kv_fp8_pool_bytes: bytes of an fp8 E4M3 comparison pool (256-byte records)."""
     n = ctypes.c_size_t()

@@ -60,7 +60,42 @@ __device__ __forceinline__ void place_code(int e, uint32_t c, uint32_t (&w)[3]) 
     }
 }
 
-template <typename T>
+// turbo5k K (template FMT = kFmtT5k, K vectors only): after the same rotation,
+// per 128-dim half (lanes 16h .. 16h + 15) the fp16 root-mean-square scale
+// (float32 squares summed from each lane's first element on, then over lane
+// pairs 1, 2, 4, 8 apart), codes = the number of boundaries below y / s, and a
+// 164-byte record: low nibbles (4 bytes per lane), 5th bits (1 byte per lane),
+// the two scales.
+__device__ __forceinline__ void t5k_encode_store(const float (&x)[8], int lane, const T5kTable& tab, uint8_t* rec,
+                                                 bool& overflow) {
+    float acc = __fmul_rn(x[0], x[0]);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) acc = __fadd_rn(acc, __fmul_rn(x[i], x[i]));
+#pragma unroll
+    for (int m = 1; m < 16; m <<= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, m));
+    const __half s16 = __float2half_rn(__fsqrt_rn(__fmul_rn(acc, 0.0078125f)));
+    const float s = __half2float(s16);
+    overflow = isinf(s);
+    uint32_t nib = 0u, top = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t c = 16u;
+        if (s != 0.0f) {
+            const float v = __fdiv_rn(x[i], s);
+            c = 0u;
+#pragma unroll
+            for (int step = 16; step >= 1; step >>= 1)   // boundaries below v, by bisection
+                if (c + step - 1 < 31u && v > tab.b[c + step - 1]) c += step;
+        }
+        nib |= (c & 0xFu) << (4 * i);
+        top |= (c >> 4) << i;
+    }
+    reinterpret_cast<uint32_t*>(rec)[lane] = nib;
+    rec[128 + lane] = (uint8_t)top;
+    if ((lane & 15) == 0) reinterpret_cast<__half*>(rec + 160)[lane >> 4] = s16;
+}
+
+template <typename T, int FMT>
 __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
     // launched with programmatic stream serialisation: let the next grid be
     // scheduled, and wait for the previous one before reading anything
@@ -126,6 +161,21 @@ __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) x[i] = __fmul_rn(x[i], 0.0625f);
 
+        if (FMT == kFmtT5k && kv == 0) {
+            bool overflow = false;
+            t5k_encode_store(x, lane, a.t5k,
+                             a.pool + t5k_offset(a.num_layers, a.num_kv_heads, page, a.layer, head, 0,
+                                                 (int)(pos % kPageSize)),
+                             overflow);
+            const bool any_nonfinite = __any_sync(0xffffffffu, !finite);
+            const bool any_overflow = __any_sync(0xffffffffu, overflow);
+            if (lane == 0 && a.status) {
+                if (any_nonfinite) atomicOr(a.status, Q3KV_STATUS_NONFINITE_INPUT);
+                else if (any_overflow) atomicOr(a.status, Q3KV_STATUS_SCALE_OVERFLOW);
+            }
+            continue;
+        }
+
         // block absmax over 4 lanes
         float amax = 0.0f;
 #pragma unroll
@@ -160,8 +210,11 @@ __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
             else if (any_overflow) atomicOr(a.status, Q3KV_STATUS_SCALE_OVERFLOW);
         }
 
-        uint8_t* rec = a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, head, kv,
-                                              (int)(pos % kPageSize));
+        uint8_t* rec = a.pool + (FMT == kFmtT5k
+                                     ? t5k_offset(a.num_layers, a.num_kv_heads, page, a.layer, head, kv,
+                                                  (int)(pos % kPageSize))
+                                     : record_offset(a.num_layers, a.num_kv_heads, page, a.layer, head, kv,
+                                                     (int)(pos % kPageSize)));
         const int blk = lane >> 2;
         const int k = lane & 3;
         if (k < 3) reinterpret_cast<uint32_t*>(rec)[3 * blk + k] = w[k];
@@ -182,8 +235,12 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (a.dtype == Q3KV_F32) return cudaLaunchKernelEx(&cfg, append_kernel<float>, a);
-    return cudaLaunchKernelEx(&cfg, append_kernel<__nv_bfloat16>, a);
+    if (a.fmt == kFmtT5k) {
+        if (a.dtype == Q3KV_F32) return cudaLaunchKernelEx(&cfg, append_kernel<float, kFmtT5k>, a);
+        return cudaLaunchKernelEx(&cfg, append_kernel<__nv_bfloat16, kFmtT5k>, a);
+    }
+    if (a.dtype == Q3KV_F32) return cudaLaunchKernelEx(&cfg, append_kernel<float, kFmtQ3>, a);
+    return cudaLaunchKernelEx(&cfg, append_kernel<__nv_bfloat16, kFmtQ3>, a);
 }
 
 }  // namespace q3kv

@@ -215,6 +215,8 @@ int append_impl(int fmt, void* stream, const q3kv_cache_desc* desc, void* d_pool
     a.v = v;
     a.dtype = dtype;
     a.status = d_status;
+    a.fmt = fmt;
+    if (fmt == kFmtT5k) a.t5k = t5k_table();
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     return cuda_status(fmt == kFmtFp8 ? launch_append_fp8(a, st) : launch_append(a, st));
 }
@@ -234,6 +236,10 @@ int verify_impl(int fmt, void* stream, const q3kv_cache_desc* desc, const void* 
     if (max_n_q > max_tokens) return Q3KV_ERR_UNSUPPORTED;
     if (impl < Q3KV_IMPL_AUTO || impl > Q3KV_IMPL_MMA) return Q3KV_ERR_INVALID_ARG;
     if (fmt == kFmtFp8 && impl == Q3KV_IMPL_FMA) return Q3KV_ERR_UNSUPPORTED;   // tensor-core leg only
+    if (fmt == kFmtT5k) {                                                       // CUDA-core leg only
+        if (impl == Q3KV_IMPL_MMA) return Q3KV_ERR_UNSUPPORTED;
+        impl = Q3KV_IMPL_FMA;
+    }
     Plan p;
     e = make_plan(desc, num_slots, max_ctx_len, max_n_q, impl, split_positions, &p, max_tokens);
     if (e != Q3KV_OK) return e;
@@ -272,6 +278,7 @@ int verify_impl(int fmt, void* stream, const q3kv_cache_desc* desc, const void* 
     a.part_ml = p.part_ml_bytes ? reinterpret_cast<float*>(ws + p.part_o_bytes) : nullptr;
     a.q_prep = p.q_prep_bytes ? static_cast<void*>(ws + p.part_o_bytes + p.part_ml_bytes) : nullptr;
     a.fmt = fmt;
+    if (fmt == kFmtT5k) a.t5k = t5k_table();
     a.status = d_status;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool mma = (p.impl == Q3KV_IMPL_MMA);
@@ -336,6 +343,32 @@ int q3kv_fp8_verify_attn(void* stream, const q3kv_cache_desc* desc, const void* 
                          int32_t max_n_q, int32_t layer, const void* q, int32_t dtype, float* out, int32_t impl,
                          int32_t split_positions, void* d_workspace, size_t workspace_bytes, int32_t* d_status) {
     return verify_impl(kFmtFp8, stream, desc, d_pool, d_page_table, max_pages_per_slot, d_ctx_len, d_n_q,
+                       d_q_offsets, num_slots, max_ctx_len, max_n_q, layer, q, dtype, out, impl, split_positions,
+                       d_workspace, workspace_bytes, d_status);
+}
+
+int q3kv_t5k_pool_bytes(const q3kv_cache_desc* desc, size_t* bytes) {
+    int e = check_desc(desc);
+    if (e != Q3KV_OK) return e;
+    if (!bytes) return Q3KV_ERR_INVALID_ARG;
+    *bytes = (size_t)desc->num_pages * desc->num_layers * desc->num_kv_heads * kT5kChunkBytes;
+    return Q3KV_OK;
+}
+
+int q3kv_t5k_append(void* stream, const q3kv_cache_desc* desc, void* d_pool, const int32_t* d_page_table,
+                    int32_t max_pages_per_slot, const int32_t* d_slot_len, const int32_t* d_n_new,
+                    const int32_t* d_row_offsets, int32_t num_slots, int32_t max_n_new, int32_t layer,
+                    const void* k, const void* v, int32_t dtype, int32_t* d_status) {
+    return append_impl(kFmtT5k, stream, desc, d_pool, d_page_table, max_pages_per_slot, d_slot_len, d_n_new,
+                       d_row_offsets, num_slots, max_n_new, layer, k, v, dtype, d_status);
+}
+
+int q3kv_t5k_verify_attn(void* stream, const q3kv_cache_desc* desc, const void* d_pool,
+                         const int32_t* d_page_table, int32_t max_pages_per_slot, const int32_t* d_ctx_len,
+                         const int32_t* d_n_q, const int32_t* d_q_offsets, int32_t num_slots, int64_t max_ctx_len,
+                         int32_t max_n_q, int32_t layer, const void* q, int32_t dtype, float* out, int32_t impl,
+                         int32_t split_positions, void* d_workspace, size_t workspace_bytes, int32_t* d_status) {
+    return verify_impl(kFmtT5k, stream, desc, d_pool, d_page_table, max_pages_per_slot, d_ctx_len, d_n_q,
                        d_q_offsets, num_slots, max_ctx_len, max_n_q, layer, q, dtype, out, impl, split_positions,
                        d_workspace, workspace_bytes, d_status);
 }

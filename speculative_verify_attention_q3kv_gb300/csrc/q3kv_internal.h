@@ -20,9 +20,31 @@ constexpr int kMaxRows = kGroup * kMaxNq;
 
 constexpr int kFp8RecordBytes = 256;  // fp8 E4M3 comparison format: one byte per element
 
-// Cache formats: the 3-bit rotated codec, and the fp8 E4M3 comparison format.
+// Cache formats: the 3-bit rotated codec, the fp8 E4M3 comparison format, and
+// the turbo5k-style format (5-bit Lloyd-Max K, 3-bit V).
 constexpr int kFmtQ3 = 0;
 constexpr int kFmtFp8 = 1;
+constexpr int kFmtT5k = 2;
+
+// turbo5k layout: per (page, layer, kv head) 256 K records of 164 bytes
+// (128 bytes of low code nibbles, 32 bytes of 5th code bits, 2 fp16 scales)
+// then 256 V records of the 3-bit codec's 112 bytes.
+constexpr int kT5kKRecordBytes = 164;
+constexpr size_t kT5kChunkBytes = (size_t)kPageSize * (kT5kKRecordBytes + kRecordBytes);
+__host__ __device__ inline size_t t5k_offset(int num_layers, int num_kv_heads, int64_t page, int layer,
+                                             int kv_head, int kv, int row) {
+    const size_t base = (size_t)((page * num_layers + layer) * num_kv_heads + kv_head) * kT5kChunkBytes;
+    return kv == 0 ? base + (size_t)row * kT5kKRecordBytes
+                   : base + (size_t)kPageSize * kT5kKRecordBytes + (size_t)row * kRecordBytes;
+}
+
+// The 32 float32 Lloyd-Max centroids of N(0, 1) and the 31 float32 midpoints
+// between neighbours (turbo5k K codes), computed once on the host.
+struct T5kTable {
+    float c[32];
+    float b[31];
+};
+const T5kTable& t5k_table();
 
 // Byte offset of a record inside the pool (see q3kv_pool_bytes); records of
 // rec_bytes bytes (112 for the 3-bit codec, 256 for fp8).
@@ -56,8 +78,9 @@ struct VerifyArgs {
     float* part_o;             // [slots, kv_heads, row_chunks, splits, rows_per_chunk, 256]
     float* part_ml;            // [slots, kv_heads, row_chunks, splits, rows_per_chunk, 2]
     void* q_prep;              // tensor-core leg: [unit][hi|lo][64 x 256] fp16 (rotated) queries
-    int32_t fmt;               // kFmtQ3 or kFmtFp8
+    int32_t fmt;               // kFmtQ3, kFmtFp8 or kFmtT5k
     int32_t* status;
+    T5kTable t5k;              // turbo5k only
 };
 
 struct AppendArgs {
@@ -77,6 +100,8 @@ struct AppendArgs {
     const void* v;
     int32_t dtype;
     int32_t* status;
+    int32_t fmt;               // kFmtQ3 or kFmtT5k (fp8 has its own kernel)
+    T5kTable t5k;              // turbo5k only
 };
 
 // Greedy acceptance of a verify step (argmax kernel + acceptance kernel).

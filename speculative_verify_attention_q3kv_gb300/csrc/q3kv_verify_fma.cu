@@ -1,4 +1,6 @@
-// Verify attention, CUDA-core fp32 leg (the reference flash-decode leg).
+// Verify attention, CUDA-core fp32 leg (the reference flash-decode leg); also
+// the leg that reads the turbo5k-style cache (template FMT = kFmtT5k: 5-bit
+// Lloyd-Max K records, 3-bit V records, in that format's page layout).
 //
 // Source: "Quasar" (q27 wiki), "Self-speculation as the whole design" (one
 // shared-KV verify of all drafted tokens), the Defaults paragraph of
@@ -54,7 +56,25 @@ __device__ __forceinline__ void decode_block(const uint8_t* rec, int b, float* d
     dst[31] = ((float)c31 - 3.5f) * s;
 }
 
-template <typename TIn>
+// turbo5k K: the 32 elements of block b (dims 32 b ..) from the low nibbles,
+// the 5th-bit plane and the scale of their 128-dim half: c_code * s.
+__device__ __forceinline__ void decode_t5k_block(const uint8_t* rec, int b, const T5kTable& tab, float* dst) {
+    const uint32_t* nib = reinterpret_cast<const uint32_t*>(rec) + 4 * b;        // 16 bytes: 32 nibbles
+    const uint32_t top = reinterpret_cast<const uint32_t*>(rec + 128)[b];       // 32 fifth bits
+    const float s = __half2float(reinterpret_cast<const __half*>(rec + 160)[b >> 2]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t w = nib[j];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int d = 8 * j + e;
+            const uint32_t c = ((w >> (4 * e)) & 0xFu) | (((top >> d) & 1u) << 4);
+            dst[d] = tab.c[c] * s;
+        }
+    }
+}
+
+template <typename TIn, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) verify_fma_kernel(VerifyArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     FmaSmem& sm = *reinterpret_cast<FmaSmem*>(smem_raw);
@@ -131,10 +151,17 @@ __global__ void __launch_bounds__(kThreads, 1) verify_fma_kernel(VerifyArgs a) {
                 if (page < 0 || page >= a.num_pages) { ok = false; bad_page = true; }
             }
             if (ok) {
-                const uint8_t* rk = a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, 0, pos % kPageSize);
-                const uint8_t* rv = a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, 1, pos % kPageSize);
-                decode_block(rk, b, kv_k);
-                decode_block(rv, b, kv_v);
+                if (FMT == kFmtT5k) {
+                    decode_t5k_block(a.pool + t5k_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, 0, pos % kPageSize),
+                                     b, a.t5k, kv_k);
+                    decode_block(a.pool + t5k_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, 1, pos % kPageSize),
+                                 b, kv_v);
+                } else {
+                    const uint8_t* rk = a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, 0, pos % kPageSize);
+                    const uint8_t* rv = a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, 1, pos % kPageSize);
+                    decode_block(rk, b, kv_k);
+                    decode_block(rv, b, kv_v);
+                }
             } else {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) { kv_k[e] = 0.0f; kv_v[e] = 0.0f; }
@@ -263,20 +290,24 @@ __global__ void __launch_bounds__(kThreads, 1) verify_fma_kernel(VerifyArgs a) {
 
 }  // namespace
 
-cudaError_t launch_verify_fma(const VerifyArgs& a, cudaStream_t stream) {
+namespace {
+template <typename TIn, int FMT>
+cudaError_t launch_fma_typed(const VerifyArgs& a, cudaStream_t stream) {
     const size_t smem = sizeof(FmaSmem);
-    dim3 grid((unsigned)a.num_splits, (unsigned)(a.num_kv_heads * a.row_chunks), (unsigned)a.num_slots);
-    cudaError_t e;
-    if (a.dtype == Q3KV_F32) {
-        e = cudaFuncSetAttribute(verify_fma_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        verify_fma_kernel<float><<<grid, kThreads, smem, stream>>>(a);
-    } else {
-        e = cudaFuncSetAttribute(verify_fma_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        verify_fma_kernel<__nv_bfloat16><<<grid, kThreads, smem, stream>>>(a);
-    }
+    const dim3 grid((unsigned)a.num_splits, (unsigned)(a.num_kv_heads * a.row_chunks), (unsigned)a.num_slots);
+    const cudaError_t e =
+        cudaFuncSetAttribute(verify_fma_kernel<TIn, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    verify_fma_kernel<TIn, FMT><<<grid, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_verify_fma(const VerifyArgs& a, cudaStream_t stream) {
+    const bool f32 = a.dtype == Q3KV_F32;
+    if (a.fmt == kFmtT5k)
+        return f32 ? launch_fma_typed<float, kFmtT5k>(a, stream) : launch_fma_typed<__nv_bfloat16, kFmtT5k>(a, stream);
+    return f32 ? launch_fma_typed<float, kFmtQ3>(a, stream) : launch_fma_typed<__nv_bfloat16, kFmtQ3>(a, stream);
 }
 
 }  // namespace q3kv
