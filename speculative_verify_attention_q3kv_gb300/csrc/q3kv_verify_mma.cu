@@ -80,6 +80,8 @@
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
+#include <atomic>
+
 #include "q3kv_common.cuh"
 #include "q3kv_internal.h"
 
@@ -1170,13 +1172,13 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
 }
 
 template <typename TIn, int FMT>
-cudaError_t launch_typed(const VerifyArgs& a, cudaStream_t stream, bool& attr_set) {
+cudaError_t launch_typed(const VerifyArgs& a, cudaStream_t stream, std::atomic<bool>& attr_set) {
     const size_t smem = sizeof(MmaSmem<FMT>);
-    if (!attr_set) {
+    if (!attr_set.load(std::memory_order_acquire)) {
         const cudaError_t e = cudaFuncSetAttribute(verify_mma_kernel<TIn, FMT>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set.store(true, std::memory_order_release);
     }
     const unsigned units = (unsigned)(a.num_slots * a.num_kv_heads * a.row_chunks);
     cudaLaunchAttribute attr[1];
@@ -1207,7 +1209,13 @@ cudaError_t launch_typed(const VerifyArgs& a, cudaStream_t stream, bool& attr_se
 }  // namespace
 
 cudaError_t launch_verify_mma(const VerifyArgs& a, cudaStream_t stream) {
-    static bool attr_set[4] = {false, false, false, false};
+    // the shared-memory opt-in is a per-device function attribute: one flag per
+    // (device, instantiation)
+    constexpr int kMaxDevices = 64;
+    static std::atomic<bool> flags[kMaxDevices][4];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::atomic<bool>* attr_set = flags[dev];
     const bool f32 = a.dtype == Q3KV_F32;
     if (a.fmt == kFmtFp8)
         return f32 ? launch_typed<float, kFmtFp8>(a, stream, attr_set[2])
