@@ -40,7 +40,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one verify-kernel launch, from one ncu capture of
 # this benchmark's launch configuration (profiles/verify_mma_workload2_ctx32768_t6.md);
 # workloads without a capture of the current kernel report null.
-NCU_TRAFFIC_BYTES = {2: 14913280}
+NCU_TRAFFIC_BYTES = {2: 14988288}
 L2_FLUSH_BYTES = 256 << 20
 
 
