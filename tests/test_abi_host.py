@@ -172,3 +172,24 @@ def test_nucleus_argument_checks(lib):
     for top_p in (0.0, -0.5, 1.5, float("nan")):
         assert lib.q3kv_accept_sample_nucleus(None, p, 0, 100, p, p, p, 1, 1, 1, p, 1.0, top_p, p, 1,
                                               p, p, p, None, 0, None) == _lib.Q3KV_ERR_INVALID_ARG
+
+
+def test_prefill_and_t5k_host_checks(lib):
+    d = api.make_desc(2, 2, 40)
+    # prefill: the token bound is 8,192 (the verify call keeps 16); explicit splits need no device
+    n_small = api.prefill_workspace_bytes(d, 1, 9000, 1000, _lib.Q3KV_IMPL_FMA, 256)
+    n_big = api.prefill_workspace_bytes(d, 1, 9000, 8192, _lib.Q3KV_IMPL_FMA, 256)
+    assert 0 < n_small < n_big
+    with pytest.raises(_lib.Q3KVError) as e:
+        api.prefill_workspace_bytes(d, 1, 9000, 8193, _lib.Q3KV_IMPL_FMA, 256)
+    assert e.value.code == _lib.Q3KV_ERR_INVALID_ARG
+    # turbo5k pool: 164-byte K and 112-byte V records per (page, layer, head, row)
+    n = ctypes.c_size_t()
+    assert lib.q3kv_t5k_pool_bytes(ctypes.byref(d), ctypes.byref(n)) == 0
+    assert n.value == 40 * 2 * 2 * 256 * (164 + 112)
+    # the turbo5k cache is read by the CUDA-core leg only
+    args = [None, ctypes.byref(d), None, None, 4, None, None, None, 1, 1000, 4, 0, None, 0, None,
+            _lib.Q3KV_IMPL_MMA, 256, None, 0, None]
+    assert lib.q3kv_t5k_verify_attn(*args) == _lib.Q3KV_ERR_UNSUPPORTED
+    assert lib.q3kv_t5k_append(None, ctypes.byref(d), None, None, 4, None, None, None, 1, 1, 5, None, None, 0,
+                               None) == _lib.Q3KV_ERR_INVALID_ARG        # a layer outside the pool
