@@ -58,6 +58,7 @@ extern "C" {
 #define Q3KV_ERR_WORKSPACE_TOO_SMALL -4
 #define Q3KV_ERR_CUDA               -5
 #define Q3KV_ERR_SLOT_RANGE         -6
+#define Q3KV_ERR_HOST_MEMORY        -7   /* host allocation of the page allocator failed */
 
 /* device status bits (*d_status) */
 #define Q3KV_STATUS_NONFINITE_INPUT  1
@@ -119,7 +120,9 @@ Q3KV_API int q3kv_pool_bytes(const q3kv_cache_desc* desc, size_t* bytes);
 typedef struct q3kv_allocator q3kv_allocator;
 
 /* Create an allocator over page ids [0, num_pages) for num_slots slots whose
- * page-table rows hold max_pages_per_slot entries.  *out receives the handle. */
+ * page-table rows hold max_pages_per_slot entries.  *out receives the handle.
+ * Q3KV_ERR_HOST_MEMORY if its host arrays cannot be allocated (no C++
+ * exception leaves any call of this library). */
 Q3KV_API int q3kv_allocator_create(int32_t num_pages, int32_t num_slots, int32_t max_pages_per_slot,
                           q3kv_allocator** out);
 Q3KV_API void q3kv_allocator_destroy(q3kv_allocator* a);
@@ -128,7 +131,7 @@ Q3KV_API void q3kv_allocator_destroy(q3kv_allocator* a);
  * new pages from the free list.  Writes the slot's page ids into the caller's
  * host row h_page_table_row[0 .. *n_pages_out) (length max_pages_per_slot;
  * entries past the count are set to -1).  Never shrinks.  All or nothing: on
- * Q3KV_ERR_OUT_OF_PAGES nothing changes. */
+ * Q3KV_ERR_OUT_OF_PAGES or Q3KV_ERR_HOST_MEMORY nothing changes. */
 Q3KV_API int q3kv_alloc_pages(q3kv_allocator* a, int32_t slot, int64_t n_positions,
                      int32_t* h_page_table_row, int32_t* n_pages_out);
 

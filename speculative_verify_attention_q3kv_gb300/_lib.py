@@ -23,6 +23,7 @@ Q3KV_ERR_OUT_OF_PAGES = -3
 Q3KV_ERR_WORKSPACE_TOO_SMALL = -4
 Q3KV_ERR_CUDA = -5
 Q3KV_ERR_SLOT_RANGE = -6
+Q3KV_ERR_HOST_MEMORY = -7
 
 Q3KV_STATUS_NONFINITE_INPUT = 1
 Q3KV_STATUS_SCALE_OVERFLOW = 2

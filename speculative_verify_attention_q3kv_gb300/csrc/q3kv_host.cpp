@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <memory>
 #include <new>
 #include <vector>
 
@@ -119,6 +120,7 @@ const char* q3kv_strerror(int err) {
         case Q3KV_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
         case Q3KV_ERR_CUDA: return "CUDA error";
         case Q3KV_ERR_SLOT_RANGE: return "slot index out of range";
+        case Q3KV_ERR_HOST_MEMORY: return "host memory allocation failed";
         default: return "unknown error";
     }
 }
@@ -131,17 +133,23 @@ int q3kv_pool_bytes(const q3kv_cache_desc* desc, size_t* bytes) {
     return Q3KV_OK;
 }
 
+// No C++ exception leaves these functions: a failed host allocation is
+// returned as Q3KV_ERR_HOST_MEMORY with the allocator unchanged.
 int q3kv_allocator_create(int32_t num_pages, int32_t num_slots, int32_t max_pages_per_slot, q3kv_allocator** out) {
     if (!out || num_pages <= 0 || num_slots <= 0 || max_pages_per_slot <= 0) return Q3KV_ERR_INVALID_ARG;
-    q3kv_allocator* a = new (std::nothrow) q3kv_allocator();
-    if (!a) return Q3KV_ERR_INVALID_ARG;
-    a->num_pages = num_pages;
-    a->num_slots = num_slots;
-    a->max_pages_per_slot = max_pages_per_slot;
-    a->free_list.resize(num_pages);
-    for (int32_t i = 0; i < num_pages; ++i) a->free_list[i] = num_pages - 1 - i;   // page 0 first
-    a->owned.resize(num_slots);
-    *out = a;
+    try {
+        std::unique_ptr<q3kv_allocator> a(new q3kv_allocator());
+        a->num_pages = num_pages;
+        a->num_slots = num_slots;
+        a->max_pages_per_slot = max_pages_per_slot;
+        // capacity num_pages from here on: returning pages never reallocates
+        a->free_list.resize(num_pages);
+        for (int32_t i = 0; i < num_pages; ++i) a->free_list[i] = num_pages - 1 - i;   // page 0 first
+        a->owned.resize(num_slots);
+        *out = a.release();
+    } catch (...) {
+        return Q3KV_ERR_HOST_MEMORY;
+    }
     return Q3KV_OK;
 }
 
@@ -156,6 +164,13 @@ int q3kv_alloc_pages(q3kv_allocator* a, int32_t slot, int64_t n_positions, int32
     std::vector<int32_t>& mine = a->owned[slot];
     const int64_t extra = need - (int64_t)mine.size();
     if (extra > (int64_t)a->free_list.size()) return Q3KV_ERR_OUT_OF_PAGES;
+    if (extra > 0) {
+        try {
+            mine.reserve((size_t)need);   // the only allocation: before anything changes
+        } catch (...) {
+            return Q3KV_ERR_HOST_MEMORY;
+        }
+    }
     for (int64_t i = 0; i < extra; ++i) {
         mine.push_back(a->free_list.back());
         a->free_list.pop_back();

@@ -47,6 +47,12 @@ def test_versions_and_strerror(lib):
     assert _lib.strerror(0) == "ok"
     assert "page" in _lib.strerror(_lib.Q3KV_ERR_OUT_OF_PAGES)
     assert _lib.strerror(12345) == "unknown error"
+    # every error code the header defines has its own text
+    text = open(HEADER).read()
+    codes = [int(v) for v in re.findall(r"#define\s+Q3KV_ERR_[A-Z_]+\s+(-?\d+)", text)]
+    assert _lib.Q3KV_ERR_HOST_MEMORY in codes
+    texts = [_lib.strerror(c) for c in codes]
+    assert "unknown error" not in texts and len(set(texts)) == len(codes)
 
 
 def test_pool_bytes():
