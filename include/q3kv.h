@@ -142,6 +142,10 @@ Q3KV_API int q3kv_free_slot(q3kv_allocator* a, int32_t slot);
 Q3KV_API int q3kv_free_pages(const q3kv_allocator* a, int32_t* n_free);
 
 /* ---- quantise-append --------------------------------------------------------
+ * Source: the "turbo3 3-bit KV cache" bullet of the "Quasar" (q27) wiki (each
+ * step's K and V are WHT-rotated and stored as 3-bit blocks in the slot's
+ * cache) and the PagedAttention paragraph of its prefix-reuse section (the
+ * attention KV is an append-only log addressed by position).
  * Encodes new raw K and V head vectors and writes their records.  Slot b
  * appends d_n_new[b] tokens at positions [d_slot_len[b], d_slot_len[b] +
  * d_n_new[b]); token t of slot b is input row d_row_offsets[b] + t.
@@ -161,6 +165,10 @@ Q3KV_API int q3kv_append(void* stream, const q3kv_cache_desc* desc, void* d_pool
                 const void* k, const void* v, int32_t dtype, int32_t* d_status);
 
 /* ---- verify attention ------------------------------------------------------
+ * Source: "Self-speculation as the whole design" (the step's drafts are
+ * checked in one pass over the shared KV, causal among themselves), "Width-12
+ * verify" (a few to a dozen query tokens per slot) and "Continuous batching"
+ * (ragged slots in one launch) of the "Quasar" (q27) wiki.
  * For slot b with L_b = d_ctx_len[b] positions already in the cache (the new
  * tokens appended) and T_b = d_n_q[b] query tokens, query token t in [0, T_b)
  * of q head h attends to positions [0, L_b - T_b + t] of kv head h / 8:
