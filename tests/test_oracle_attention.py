@@ -8,6 +8,8 @@
 * GQA mapping: q heads 8g..8g+7 read kv head g;
 * split invariance of the flash-decode merge rule, including fully masked rows;
 * the scores are rotation invariant: (Hq).(k_rot) = q.(H k_rot).
+* a prefill-sized case equals torch's scaled_dot_product_attention (float64,
+  explicit bottom-right causal mask, repeated kv heads).
 """
 import math
 
@@ -120,3 +122,24 @@ def test_scores_rotation_invariant():
     a = attention.scores_rotated(rotate_f64(q), k_rot)
     b = q @ rotate_f64(k_rot).T / 16.0
     np.testing.assert_allclose(a, b, atol=1e-12)
+
+
+def test_prefill_shape_equals_library_attention():
+    # A prefill-sized case (300 new tokens over 200 cached positions) against
+    # torch's scaled_dot_product_attention in float64 on the CPU (a library
+    # routine): queries rotated by scipy's Hadamard matrix, kv head repeated
+    # over its 8 q heads, row t allowed positions [0, 200 + t], output rotated
+    # back.
+    torch = __import__("torch")
+    rng = np.random.default_rng(7)
+    T, n_ctx = 300, 200
+    q, kh, vh = _case(rng, T=T, n_ctx=n_ctx, scale=2.0)
+    got = attention.verify_attention(q, kh, vh, n_ctx, 8)
+    Hs = torch.from_numpy(scipy.linalg.hadamard(256).astype(np.float64) / 16.0)
+    qr = torch.from_numpy(q).permute(1, 0, 2) @ Hs.T                       # [Hq, T, 256]
+    k = torch.from_numpy(kh).repeat_interleave(8, dim=0)                    # [Hq, L, 256]
+    v = torch.from_numpy(vh).repeat_interleave(8, dim=0)
+    allowed = torch.arange(n_ctx + T)[None, :] <= (n_ctx + torch.arange(T))[:, None]
+    o = torch.nn.functional.scaled_dot_product_attention(qr, k, v, attn_mask=allowed, scale=1.0 / 16.0)
+    want = (o @ Hs.T).permute(1, 0, 2).numpy()
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-11)
