@@ -40,6 +40,96 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"q3kv inputs must be float32 or bfloat16, got {t.dtype}")
 
 
+def _on_gpu(name: str, t: Optional[torch.Tensor], dev: int, dtype=None, min_numel: int = 0,
+            optional: bool = False) -> None:
+    """Refuse, before any launch, a tensor the kernels could not address safely.
+
+    The C ABI takes raw device pointers; a host tensor, a tensor on another
+    device, a wrong element type or a buffer shorter than the call's counts
+    would be read or written out of bounds on the GPU.  Values inside device
+    arrays (lengths, offsets, page ids) are checked by the kernels.
+    """
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    idx = _device_index(t)
+    if idx is None:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if idx != dev:
+        raise ValueError(f"{name} is on cuda:{idx}, the current device is cuda:{dev}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.numel() < min_numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, the call needs at least {min_numel}")
+
+
+def _device_index(t: torch.Tensor) -> Optional[int]:
+    """CUDA device index of a tensor; None for a tensor in host (or any other) memory."""
+    return t.device.index if t.is_cuda else None
+
+
+def _current_device() -> int:
+    return torch.cuda.current_device() if torch.cuda.is_available() else -1
+
+
+def _nbytes(t: torch.Tensor) -> int:
+    return t.numel() * t.element_size()
+
+
+def _check_cache_args(desc: CacheDesc, pool: torch.Tensor, need_pool_bytes: int, page_table: torch.Tensor,
+                      lens: torch.Tensor, counts: torch.Tensor, offsets: torch.Tensor,
+                      status: Optional[torch.Tensor], dev: int) -> int:
+    """Common checks of the append / verify / prefill calls; returns num_slots."""
+    _on_gpu("pool", pool, dev)
+    if _nbytes(pool) < need_pool_bytes:
+        raise ValueError(f"pool holds {_nbytes(pool)} bytes, the cache needs {need_pool_bytes}")
+    _on_gpu("lengths", lens, dev, torch.int32)
+    if lens.dim() != 1:
+        raise ValueError("per-slot lengths must be one-dimensional")
+    n = lens.shape[0]
+    _on_gpu("page_table", page_table, dev, torch.int32)
+    if page_table.dim() != 2 or page_table.shape[1] < 1 or (n > 0 and page_table.shape[0] < n):
+        raise ValueError(f"page_table must be int32 [num_slots >= {n}, max_pages_per_slot >= 1], "
+                         f"got {tuple(page_table.shape)}")
+    _on_gpu("per-slot token counts", counts, dev, torch.int32, n)
+    _on_gpu("row offsets", offsets, dev, torch.int32, n)
+    _on_gpu("status", status, dev, torch.int32, 1, optional=True)
+    return n
+
+
+def _check_rows(name: str, t: torch.Tensor, heads: int, dev: int) -> None:
+    _on_gpu(name, t, dev)
+    if t.dim() != 3 or t.shape[1] != heads or t.shape[2] != HEAD_DIM:
+        raise ValueError(f"{name} must be [rows, {heads}, {HEAD_DIM}], got {tuple(t.shape)}")
+
+
+def _check_append(desc, pool, pool_bytes_fn, page_table, slot_len, n_new, row_offsets, k, v, status) -> None:
+    dev = _current_device()
+    _check_cache_args(desc, pool, pool_bytes_fn(desc), page_table, slot_len, n_new, row_offsets, status, dev)
+    if k.dtype != v.dtype:
+        raise TypeError("k and v must share a dtype")
+    _check_rows("k", k, desc.num_kv_heads, dev)
+    _check_rows("v", v, desc.num_kv_heads, dev)
+    if k.shape != v.shape:
+        raise ValueError(f"k and v differ in shape: {tuple(k.shape)} vs {tuple(v.shape)}")
+
+
+def _check_verify(desc, pool, pool_bytes_fn, page_table, ctx_len, n_q, q_offsets, q, out, workspace,
+                  status) -> None:
+    dev = _current_device()
+    _check_cache_args(desc, pool, pool_bytes_fn(desc), page_table, ctx_len, n_q, q_offsets, status, dev)
+    _check_rows("q", q, desc.num_q_heads, dev)
+    if out.dtype != torch.float32:
+        raise TypeError("out must be float32")
+    _check_rows("out", out, desc.num_q_heads, dev)
+    if out.shape[0] < q.shape[0]:
+        raise ValueError(f"out has {out.shape[0]} rows, q has {q.shape[0]}")
+    _on_gpu("workspace", workspace, dev, optional=True)
+
+
 def _stream(stream) -> int:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -103,8 +193,7 @@ def append(desc: CacheDesc, pool: torch.Tensor, page_table: torch.Tensor, slot_l
            n_new: torch.Tensor, row_offsets: torch.Tensor, max_n_new: int, layer: int,
            k: torch.Tensor, v: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None) -> None:
     """q3kv_append: quantise and store k, v [rows, kv_heads, 256] for each slot."""
-    if k.dtype != v.dtype:
-        raise TypeError("k and v must share a dtype")
+    _check_append(desc, pool, pool_bytes, page_table, slot_len, n_new, row_offsets, k, v, status)
     rc = _lib.load().q3kv_append(_stream(stream), ctypes.byref(desc), _ptr(pool), _ptr(page_table),
                                  page_table.shape[1], _ptr(slot_len), _ptr(n_new), _ptr(row_offsets),
                                  slot_len.shape[0], max_n_new, layer, _ptr(k), _ptr(v), _dtype_code(k),
@@ -118,8 +207,7 @@ def verify_attn(desc: CacheDesc, pool: torch.Tensor, page_table: torch.Tensor, c
                 impl: int = _lib.Q3KV_IMPL_AUTO, split_positions: int = 0,
                 status: Optional[torch.Tensor] = None, stream=None) -> None:
     """q3kv_verify_attn: out[rows, q_heads, 256] (float32) for every slot's query tokens."""
-    if out.dtype != torch.float32:
-        raise TypeError("out must be float32")
+    _check_verify(desc, pool, pool_bytes, page_table, ctx_len, n_q, q_offsets, q, out, workspace, status)
     rc = _lib.load().q3kv_verify_attn(_stream(stream), ctypes.byref(desc), _ptr(pool), _ptr(page_table),
                                       page_table.shape[1], _ptr(ctx_len), _ptr(n_q), _ptr(q_offsets),
                                       ctx_len.shape[0], max_ctx_len, max_n_q, layer, _ptr(q), _dtype_code(q),
@@ -137,8 +225,7 @@ def verify_attn_noalloc(desc: CacheDesc, pool: torch.Tensor, page_table: torch.T
     For callers that cannot provide device scratch memory; calls that overlap
     on the GPU share that scratch and must not run concurrently.
     """
-    if out.dtype != torch.float32:
-        raise TypeError("out must be float32")
+    _check_verify(desc, pool, pool_bytes, page_table, ctx_len, n_q, q_offsets, q, out, None, status)
     rc = _lib.load().q3kv_verify_attn_noalloc(_stream(stream), ctypes.byref(desc), _ptr(pool), _ptr(page_table),
                                               page_table.shape[1], _ptr(ctx_len), _ptr(n_q), _ptr(q_offsets),
                                               ctx_len.shape[0], max_ctx_len, max_n_q, layer, _ptr(q),
@@ -160,8 +247,7 @@ def prefill_attn(desc: CacheDesc, pool: torch.Tensor, page_table: torch.Tensor, 
                  impl: int = _lib.Q3KV_IMPL_AUTO, split_positions: int = 0,
                  status: Optional[torch.Tensor] = None, stream=None) -> None:
     """q3kv_prefill_attn: causal attention of up to 8192 appended tokens per slot over the 3-bit cache."""
-    if out.dtype != torch.float32:
-        raise TypeError("out must be float32")
+    _check_verify(desc, pool, pool_bytes, page_table, ctx_len, n_new, q_offsets, q, out, workspace, status)
     rc = _lib.load().q3kv_prefill_attn(_stream(stream), ctypes.byref(desc), _ptr(pool), _ptr(page_table),
                                        page_table.shape[1], _ptr(ctx_len), _ptr(n_new), _ptr(q_offsets),
                                        ctx_len.shape[0], max_ctx_len, max_n_new, layer, _ptr(q), _dtype_code(q),
@@ -181,8 +267,7 @@ def t5k_append(desc: CacheDesc, pool: torch.Tensor, page_table: torch.Tensor, sl
                n_new: torch.Tensor, row_offsets: torch.Tensor, max_n_new: int, layer: int,
                k: torch.Tensor, v: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None) -> None:
     """q3kv_t5k_append: 5-bit Lloyd-Max K and 3-bit V records for k, v [rows, kv_heads, 256]."""
-    if k.dtype != v.dtype:
-        raise TypeError("k and v must share a dtype")
+    _check_append(desc, pool, t5k_pool_bytes, page_table, slot_len, n_new, row_offsets, k, v, status)
     rc = _lib.load().q3kv_t5k_append(_stream(stream), ctypes.byref(desc), _ptr(pool), _ptr(page_table),
                                      page_table.shape[1], _ptr(slot_len), _ptr(n_new), _ptr(row_offsets),
                                      slot_len.shape[0], max_n_new, layer, _ptr(k), _ptr(v), _dtype_code(k),
@@ -196,8 +281,7 @@ def t5k_verify_attn(desc: CacheDesc, pool: torch.Tensor, page_table: torch.Tenso
                     impl: int = _lib.Q3KV_IMPL_FMA, split_positions: int = 0,
                     status: Optional[torch.Tensor] = None, stream=None) -> None:
     """q3kv_t5k_verify_attn: verify attention over the turbo5k-style cache (CUDA-core leg)."""
-    if out.dtype != torch.float32:
-        raise TypeError("out must be float32")
+    _check_verify(desc, pool, t5k_pool_bytes, page_table, ctx_len, n_q, q_offsets, q, out, workspace, status)
     rc = _lib.load().q3kv_t5k_verify_attn(_stream(stream), ctypes.byref(desc), _ptr(pool), _ptr(page_table),
                                           page_table.shape[1], _ptr(ctx_len), _ptr(n_q), _ptr(q_offsets),
                                           ctx_len.shape[0], max_ctx_len, max_n_q, layer, _ptr(q), _dtype_code(q),
@@ -217,8 +301,7 @@ def fp8_append(desc: CacheDesc, pool: torch.Tensor, page_table: torch.Tensor, sl
                n_new: torch.Tensor, row_offsets: torch.Tensor, max_n_new: int, layer: int,
                k: torch.Tensor, v: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None) -> None:
     """q3kv_fp8_append: store k, v [rows, kv_heads, 256] as E4M3 records (the comparison cache)."""
-    if k.dtype != v.dtype:
-        raise TypeError("k and v must share a dtype")
+    _check_append(desc, pool, fp8_pool_bytes, page_table, slot_len, n_new, row_offsets, k, v, status)
     rc = _lib.load().q3kv_fp8_append(_stream(stream), ctypes.byref(desc), _ptr(pool), _ptr(page_table),
                                      page_table.shape[1], _ptr(slot_len), _ptr(n_new), _ptr(row_offsets),
                                      slot_len.shape[0], max_n_new, layer, _ptr(k), _ptr(v), _dtype_code(k),
@@ -232,14 +315,35 @@ def fp8_verify_attn(desc: CacheDesc, pool: torch.Tensor, page_table: torch.Tenso
                     impl: int = _lib.Q3KV_IMPL_AUTO, split_positions: int = 0,
                     status: Optional[torch.Tensor] = None, stream=None) -> None:
     """q3kv_fp8_verify_attn: verify attention over the fp8 comparison cache (tensor-core leg)."""
-    if out.dtype != torch.float32:
-        raise TypeError("out must be float32")
+    _check_verify(desc, pool, fp8_pool_bytes, page_table, ctx_len, n_q, q_offsets, q, out, workspace, status)
     rc = _lib.load().q3kv_fp8_verify_attn(_stream(stream), ctypes.byref(desc), _ptr(pool), _ptr(page_table),
                                           page_table.shape[1], _ptr(ctx_len), _ptr(n_q), _ptr(q_offsets),
                                           ctx_len.shape[0], max_ctx_len, max_n_q, layer, _ptr(q), _dtype_code(q),
                                           _ptr(out), impl, split_positions, _ptr(workspace),
                                           workspace.numel() * workspace.element_size(), _ptr(status))
     check(rc, "q3kv_fp8_verify_attn")
+
+
+def _check_accept(logits, q_offsets, n_q, tokens, ctx_len, n_accepted, next_token, committed_len, workspace,
+                  status):
+    """Checks common to the acceptance calls; returns (rows, vocab) of the logits."""
+    dev = _current_device()
+    _on_gpu("logits", logits, dev)
+    if logits.dim() != 2:
+        raise ValueError(f"logits must be [rows, vocab], got {tuple(logits.shape)}")
+    _dtype_code(logits)
+    rows, vocab = logits.shape
+    _on_gpu("n_q", n_q, dev, torch.int32)
+    if n_q.dim() != 1:
+        raise ValueError("n_q must be one-dimensional")
+    n = n_q.shape[0]
+    for name, t in (("q_offsets", q_offsets), ("ctx_len", ctx_len), ("n_accepted", n_accepted),
+                    ("next_token", next_token), ("committed_len", committed_len)):
+        _on_gpu(name, t, dev, torch.int32, n)
+    _on_gpu("tokens", tokens, dev, torch.int32, rows)
+    _on_gpu("workspace", workspace, dev, optional=True)
+    _on_gpu("status", status, dev, torch.int32, 1, optional=True)
+    return rows, vocab
 
 
 def accept_workspace_bytes(num_rows: int, vocab: int) -> int:
@@ -253,7 +357,8 @@ def accept_greedy(logits: torch.Tensor, q_offsets: torch.Tensor, n_q: torch.Tens
                   committed_len: torch.Tensor, workspace: Optional[torch.Tensor],
                   status: Optional[torch.Tensor] = None, stream=None) -> None:
     """q3kv_accept_greedy: logits [rows, vocab] (f32 or bf16); int32 per-slot outputs."""
-    rows, vocab = logits.shape
+    rows, vocab = _check_accept(logits, q_offsets, n_q, tokens, ctx_len, n_accepted, next_token, committed_len,
+                                workspace, status)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = _lib.load().q3kv_accept_greedy(_stream(stream), _ptr(logits), _dtype_code(logits), vocab, _ptr(q_offsets),
                                         _ptr(n_q), _ptr(tokens), n_q.shape[0], rows, max_n_q, _ptr(ctx_len),
@@ -267,9 +372,9 @@ def accept_sample(logits: torch.Tensor, q_offsets: torch.Tensor, n_q: torch.Tens
                   n_accepted: torch.Tensor, next_token: torch.Tensor, committed_len: torch.Tensor,
                   workspace: Optional[torch.Tensor], status: Optional[torch.Tensor] = None, stream=None) -> None:
     """q3kv_accept_sample: rejection-sampled acceptance; uniforms float32 [rows]."""
-    rows, vocab = logits.shape
-    if uniforms.dtype != torch.float32:
-        raise TypeError("uniforms must be float32")
+    rows, vocab = _check_accept(logits, q_offsets, n_q, tokens, ctx_len, n_accepted, next_token, committed_len,
+                                workspace, status)
+    _on_gpu("uniforms", uniforms, _current_device(), torch.float32, rows)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = _lib.load().q3kv_accept_sample(_stream(stream), _ptr(logits), _dtype_code(logits), vocab, _ptr(q_offsets),
                                         _ptr(n_q), _ptr(tokens), n_q.shape[0], rows, max_n_q, _ptr(ctx_len),
@@ -285,9 +390,9 @@ def accept_sample_nucleus(logits: torch.Tensor, q_offsets: torch.Tensor, n_q: to
                           committed_len: torch.Tensor, workspace: Optional[torch.Tensor],
                           status: Optional[torch.Tensor] = None, stream=None) -> None:
     """q3kv_accept_sample_nucleus: rejection-sampled acceptance with the top-p nucleus."""
-    rows, vocab = logits.shape
-    if uniforms.dtype != torch.float32:
-        raise TypeError("uniforms must be float32")
+    rows, vocab = _check_accept(logits, q_offsets, n_q, tokens, ctx_len, n_accepted, next_token, committed_len,
+                                workspace, status)
+    _on_gpu("uniforms", uniforms, _current_device(), torch.float32, rows)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = _lib.load().q3kv_accept_sample_nucleus(_stream(stream), _ptr(logits), _dtype_code(logits), vocab,
                                                 _ptr(q_offsets), _ptr(n_q), _ptr(tokens), n_q.shape[0], rows,
