@@ -1,0 +1,52 @@
+"""The operand-precision ladder behind the tensor-core leg's design (tests/precision_ladder.py).
+
+On a reduced workload-2 case (4,096 cached positions, 6 tokens, log-uniform
+channel scales) the ladder must show what the design rests on: any single
+fp16 operand for Q or K̂ misses the 2e-3 tolerance, while the kernel's split
+scheme (exact K̂/V̂ pairs, round-to-nearest Q/P pairs, three products) and the
+fp8 leg's two-product scheme stay far inside it.  The ladder's exact row is
+tied to the oracle's attention first, so the emulation measures against the
+oracle's definition.
+"""
+import numpy as np
+
+import precision_ladder as pl
+from oracle import attention, fp8
+from oracle.cache import encode_dequantized
+
+MAX_ABS, REL_L2 = 2e-3, 1e-3
+
+
+def _case():
+    return pl.Case(2, 0, 1, 4096, 6)
+
+
+def test_ladder_reference_is_the_oracle():
+    case = _case()
+    res = pl.ladder_q3(case)
+    kh = encode_dequantized(case.k_raw)[None]
+    vh = encode_dequantized(case.v_raw)[None]
+    q = case.q_raw.reshape(6, 8, 256)
+    want = attention.verify_attention(q, kh, vh, 4096, 8).reshape(48, 256)
+    np.testing.assert_allclose(res["reference"], want, rtol=0, atol=1e-10)
+    ref8 = pl.ladder_fp8(case)["reference"]
+    k8 = fp8.decode(fp8.encode_vectors(case.k_raw)[0])[None]
+    v8 = fp8.decode(fp8.encode_vectors(case.v_raw)[0])[None]
+    np.testing.assert_allclose(ref8, fp8.attention(q, k8, v8, 4096, 8).reshape(48, 256), rtol=0, atol=1e-10)
+
+
+def test_exact_split_is_exact_in_fp16():
+    x = _case().k_raw[:300]
+    val, hi, lo = pl.exact_split_q3(x)
+    assert np.array_equal(hi + lo, val)
+    assert np.array_equal(pl.f16(hi), hi) and np.array_equal(pl.f16(lo), lo)
+
+
+def test_single_fp16_operands_miss_and_the_split_schemes_meet_the_tolerance():
+    case = _case()
+    err = pl.errors(pl.ladder_q3(case))
+    err.update(pl.errors(pl.ladder_fp8(case)))
+    for name in ("all_f16", "q_f16", "k_f16"):
+        assert err[name][0] > MAX_ABS, (name, err[name])
+    assert err["kernel_q3"][0] < MAX_ABS / 5 and err["kernel_q3"][1] < REL_L2 / 10, err["kernel_q3"]
+    assert err["kernel_fp8"][0] < MAX_ABS / 20 and err["kernel_fp8"][1] < REL_L2 / 100, err["kernel_fp8"]
