@@ -505,19 +505,24 @@ def cpu_baseline(w, budget_s=20.0):
     per_layer = spent / layers
     tokens = sum(shapes.n_new[0])
     return {"value": tokens / (per_layer * w.num_layers), "unit": "tokens/s", "cores": _threads(),
-            "kind": "oracle",
+            "host_cpus": os.cpu_count(), "blas_threads": _blas_threads(), "kind": "oracle",
             "sample": f"{layers} of {w.num_layers} layers of one step (append + verify, every slot), "
                       f"scaled to {w.num_layers} layers; prefill not timed"}
 
 
-def _threads():
+def _blas_threads():
+    """Threads of the BLAS numpy calls into (None where threadpoolctl is not installed)."""
     try:
         import threadpoolctl
 
-        n = max((p.get("num_threads", 1) for p in threadpoolctl.threadpool_info()), default=1)
-        return int(n)
+        return int(max((p.get("num_threads", 1) for p in threadpoolctl.threadpool_info()), default=1))
     except Exception:
-        return os.cpu_count() or 1
+        return None
+
+
+def _threads():
+    n = _blas_threads()
+    return n if n is not None else (os.cpu_count() or 1)
 
 
 def run_reference(args, rank, world):
@@ -538,7 +543,8 @@ def run_reference(args, rank, world):
             "config": {"workload": w.name, "slots": w.num_slots, "layers": w.num_layers, "ctx": shapes.ctx,
                        "query_tokens": shapes.n_new[0]},
             "impl": "reference",
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _threads(), "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _threads(), "host_cpus": os.cpu_count(),
+                             "blas_threads": _blas_threads(), "kind": "oracle",
                              "sample": "each step runs one layer of the step (append + verify of every slot) "
                                        "and counts it for all layers"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
