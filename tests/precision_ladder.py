@@ -24,7 +24,9 @@ The tensor-core leg's own choices, as emulated by ``kernel_q3`` and
 * fp8 E4M3 values are exact in fp16, so that format needs two products per
   contraction (Qhi.K + Qlo.K, Phi.V + Plo.V) and no rotation.
 
-Run as a script for the ladder at the workloads' full sizes (minutes of CPU):
+Workloads 3 and 4 draw K, V and Q from workload 2's distributions, so the
+ladder runs workloads 1, 2 and 5.  Run it as a script for their full sizes
+(minutes of CPU):
 
     python tests/precision_ladder.py
 """
