@@ -145,17 +145,40 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+_HBM_KEYS = ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs")
+
+
+def _find_hbm(d, depth=0):
+    """First positive HBM copy bandwidth (GB/s) in a peaks record: top-level keys first, then nested ones."""
+    if not isinstance(d, dict) or depth > 3:
+        return None
+    for key in _HBM_KEYS:
+        if key in d:
+            v = d[key]
+            v = v.get("value", v.get("gbs")) if isinstance(v, dict) else v
+            try:
+                v = float(v)
+            except (TypeError, ValueError):
+                continue
+            if v > 0:
+                return v
+    for v in d.values():
+        found = _find_hbm(v, depth + 1)
+        if found is not None:
+            return found
+    return None
+
+
 def measured_peak_hbm():
+    """(GB/s, "measured") from MEASURED_PEAKS.json next to this file, else the fallback figure."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         try:
-            d = json.load(open(p))
-            for key in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
-                if key in d:
-                    v = d[key]
-                    v = v.get("value", v) if isinstance(v, dict) else v
-                    return float(v), "measured"
-        except (ValueError, OSError, TypeError):
+            with open(p) as f:
+                v = _find_hbm(json.load(f))
+            if v is not None:
+                return v, "measured"
+        except (ValueError, OSError):
             pass
     return FALLBACK_HBM_GBS, "fallback"
 
