@@ -103,6 +103,27 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.mark_at = 0
+
+    def mark(self):
+        """Samples from the one just before this point on describe the timed region."""
+        self.mark_at = max(len(self.lines) - 1, 0)
+
+    def wait_samples(self, n, busy, timeout_s=3.0):
+        """Call busy() (untimed GPU work that it waits for) until n samples arrived after the mark.
+
+        nvidia-smi reports every 200 ms, longer than a short timed region: keeping
+        the GPU loaded until samples arrive makes them describe the clocks under
+        the benchmark's own load.  Bounded by timeout_s; never raises.
+        """
+        if self.proc is None:
+            return
+        t0 = time.monotonic()
+        try:
+            while len(self.lines) - self.mark_at < n and time.monotonic() - t0 < timeout_s:
+                busy()
+        except Exception:
+            pass
 
     def start(self):
         try:
@@ -129,7 +150,7 @@ class ClockSampler:
             self.proc.kill()
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in self.lines[self.mark_at:]:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -142,7 +163,9 @@ class ClockSampler:
                 if val.lower() == "active":
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "window": "200 ms samples from the last one before the timed region through untimed replays "
+                          "of the same step right after it"}
 
 
 _HBM_KEYS = ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs")
@@ -366,9 +389,17 @@ def run_ours(args, rank, world, local, pg):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     vev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clocks = ClockSampler(local)
+
+    def busy():                             # untimed load while the clock samples arrive
+        for _ in range(8):
+            g_step.replay()
+        torch.cuda.synchronize()
+
+    clocks.start()
+    clocks.wait_samples(1, busy)
     barrier(pg)
     torch.cuda.synchronize()
-    clocks.start()
+    clocks.mark()
     for s in range(args.steps):
         flush.zero_()                       # L2 flush between timed steps (outside the events)
         ev[s][0].record(stream)
@@ -392,6 +423,7 @@ def run_ours(args, rank, world, local, pg):
         g_nucleus.replay()                  # sampled acceptance with the top-p nucleus
         nev[s][1].record(stream)
     torch.cuda.synchronize()
+    clocks.wait_samples(3, busy)
     clock_info = clocks.stop()
     barrier(pg)
     step_ms = [a.elapsed_time(b_) for a, b_ in ev]
@@ -622,9 +654,16 @@ def run_prefill(args, rank, world, local, pg):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     aev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clocks = ClockSampler(local)
+
+    def busy():                             # untimed load while the clock samples arrive
+        step()
+        torch.cuda.synchronize()
+
+    clocks.start()
+    clocks.wait_samples(1, busy)
     barrier(pg)
     torch.cuda.synchronize()
-    clocks.start()
+    clocks.mark()
     for s_ in range(args.steps):
         flush.zero_()
         ev[s_][0].record()
@@ -636,6 +675,7 @@ def run_prefill(args, rank, world, local, pg):
         step(append=False)
         aev[s_][1].record()
     torch.cuda.synchronize()
+    clocks.wait_samples(3, busy)
     clock_info = clocks.stop()
     barrier(pg)
     assert int(status.item()) == 0, "device status flagged during the prefill benchmark"
