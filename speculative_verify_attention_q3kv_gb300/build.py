@@ -34,13 +34,18 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp")))
 
 
+def dependencies():
+    """Every file the library is built from: sources, headers (.h, .cuh) and this script."""
+    deps = sources() + HEADERS + sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh")))
+    deps.append(os.path.abspath(__file__))
+    return deps
+
+
 def _stale() -> bool:
     if not os.path.exists(LIB):
         return True
     t = os.path.getmtime(LIB)
-    deps = sources() + HEADERS + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".h")]
-    deps.append(os.path.abspath(__file__))
-    return any(os.path.getmtime(p) > t for p in deps)
+    return any(os.path.getmtime(p) > t for p in dependencies())
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:

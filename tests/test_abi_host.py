@@ -199,3 +199,14 @@ def test_prefill_and_t5k_host_checks(lib):
     assert lib.q3kv_t5k_verify_attn(*args) == _lib.Q3KV_ERR_UNSUPPORTED
     assert lib.q3kv_t5k_append(None, ctypes.byref(d), None, None, 4, None, None, None, 1, 1, 5, None, None, 0,
                                None) == _lib.Q3KV_ERR_INVALID_ARG        # a layer outside the pool
+
+
+def test_build_flags_and_dependencies():
+    from speculative_verify_attention_q3kv_gb300 import build as b
+    # one sm_103a target; IEEE division and no fast-math (the codec's codes are bit-exact)
+    assert b.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert not any("fast" in f for f in b.NVFLAGS)
+    # every file in csrc (and the public header) triggers a rebuild when it changes
+    deps = set(b.dependencies())
+    assert {os.path.join(b.CSRC, f) for f in os.listdir(b.CSRC)} <= deps
+    assert HEADER in deps
