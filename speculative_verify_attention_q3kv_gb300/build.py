@@ -7,6 +7,7 @@ happens when a source or header is newer than the library.
 from __future__ import annotations
 
 import concurrent.futures
+import fcntl
 import os
 import shutil
 import subprocess
@@ -49,10 +50,26 @@ def _stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Build the library if needed; return its path."""
+    """Build the library if needed; return its path.
+
+    Processes that build at the same time (ranks of one job) take turns on a
+    lock file, and each looks again whether the library is stale once it holds
+    the lock, so the compilation runs once.
+    """
     if not force and not _stale():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and not _stale():
+                return LIB
+            return _compile(verbose, extra_flags)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _compile(verbose: bool, extra_flags) -> str:
     nvcc = _nvcc()
     objs = []
     cmds = []
