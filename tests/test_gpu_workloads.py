@@ -14,7 +14,6 @@ import torch
 
 import q3kv_inputs as qi
 from gpu_harness import GpuCache, check_close, oracle_records, oracle_verify, slot_kv
-from oracle.cache import encode_dequantized
 
 pytestmark = pytest.mark.gpu
 
