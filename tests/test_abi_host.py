@@ -210,3 +210,41 @@ def test_build_flags_and_dependencies():
     deps = set(b.dependencies())
     assert {os.path.join(b.CSRC, f) for f in os.listdir(b.CSRC)} <= deps
     assert HEADER in deps
+
+
+def _c_prototypes():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for ret, name, args in re.findall(r"Q3KV_API\s+([\w\s\*]+?)\s*\b(q3kv_\w+)\s*\((.*?)\)\s*;", text, flags=re.S):
+        args = " ".join(args.split())
+        out[name] = (" ".join(ret.split()), [] if args in ("", "void") else [a.strip() for a in args.split(",")])
+    return out
+
+
+def _ctype_class(decl):
+    """ctypes class(es) that can carry a C parameter declaration."""
+    if "*" in decl:
+        return "pointer"
+    t = decl.replace("const ", "").split()[0]
+    return {"int": ctypes.c_int32, "int32_t": ctypes.c_int32, "int64_t": ctypes.c_int64, "size_t": ctypes.c_size_t,
+            "float": ctypes.c_float, "uint64_t": ctypes.c_uint64}[t]
+
+
+def test_binding_prototypes_match_the_header():
+    protos = _c_prototypes()
+    assert set(protos) == set(_lib.PROTOTYPES)
+    for name, (ret, args) in protos.items():
+        res, argtypes = _lib.PROTOTYPES[name]
+        assert len(argtypes) == len(args), name
+        for decl, ct in zip(args, argtypes):
+            want = _ctype_class(decl)
+            if want == "pointer":
+                assert ct in (ctypes.c_void_p, ctypes.c_char_p) or issubclass(ct, ctypes._Pointer), (name, decl)
+            else:
+                assert ct is want, (name, decl, ct)
+        if ret == "void":
+            assert res is None, name
+        elif "char" in ret:
+            assert res is ctypes.c_char_p, name
+        else:
+            assert res is ctypes.c_int32 and ret == "int", (name, ret)
