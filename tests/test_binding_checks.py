@@ -164,3 +164,15 @@ def test_accept_call_rules(fake):
     with pytest.raises(ValueError, match="uniforms"):
         api.accept_sample_nucleus(lg, z, z, toks, 3, z, 1.0, 0.9, u[:3], 1, z, z, z, None)
     assert len(fake.calls) == 3
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    # no library and no build: the binding raises; there is no other path to the results
+    from speculative_verify_attention_q3kv_gb300 import build as b
+    monkeypatch.setattr(_lib, "_LIB", None)
+    monkeypatch.setattr(b, "LIB", str(tmp_path / "libq3kv.so"))
+    with pytest.raises(OSError, match="libq3kv.so not found"):
+        _lib.load(build_if_missing=False)
+    monkeypatch.setattr(b, "build", lambda *a, **k: (_ for _ in ()).throw(RuntimeError("nvcc not found")))
+    with pytest.raises(RuntimeError, match="nvcc"):
+        api.pool_bytes(api.make_desc(1, 2, 8))
