@@ -478,6 +478,7 @@ def run_ours(args, rank, world, local, pg):
         "steps": args.steps,
         "warmup": max(args.warmup, 3),
         "ms_per_step": total_s * 1e3 / args.steps,
+        "ms_per_step_median": statistics.median(step_ms),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
