@@ -16,9 +16,12 @@ The tensor-core leg's own choices, as emulated by ``kernel_q3`` and
 * Q is rotated and scaled into log2 units (H q / 16 * log2 e), then split into
   round-to-nearest fp16 hi/lo;
 * the 3-bit K/V values (c - 3.5) s are split exactly: s_hi = s with its fp16
-  mantissa cut to 6 significant bits, s_lo = s - s_hi, so (c - 3.5) s_hi and
-  (c - 3.5) s_lo are both exact in fp16;
-* S = Qhi.Khi + Qlo.Khi + Qhi.Klo (the Qlo.Klo product is dropped);
+  mantissa cut to 8 (K) or 6 (V) significant bits, s_lo = s - s_hi, so
+  (c - 3.5) s_hi and (c - 3.5) s_lo are both exact in fp16;
+* S = Qhi.Khi + Qlo.Khi + Qhi.Klo (the Qlo.Klo product is dropped: below
+  2^-20 of the scores with the 8-bit K split; a 6-bit K split left it at
+  2^-18, which on outlier-heavy queries and keys costs up to 2e-3 of output,
+  the ``kernel_q3_k6`` row);
 * P = 2^(S - max) in fp32; the row sum is taken from that fp32 P; P is split
   into round-to-nearest fp16 hi/lo and O = Phi.Vhi + Phi.Vlo + Plo.Vhi;
 * fp8 E4M3 values are exact in fp16, so that format needs two products per
@@ -59,20 +62,27 @@ def split16(x):
     return hi, f16(np.asarray(x, np.float64) - hi)
 
 
-def exact_split_q3(x_raw):
-    """3-bit K or V of raw vectors -> (value, hi, lo) with hi + lo == value exactly."""
+K_HI_MASK = 0xFFF8   # fp16 bits of s kept in s_hi for K: 8 significant bits
+V_HI_MASK = 0xFFE0   # for V: 6 significant bits
+
+
+def exact_split_q3(x_raw, hi_mask=V_HI_MASK):
+    """3-bit K or V of raw vectors -> (value, hi, lo) with hi + lo == value exactly.
+
+    s_hi keeps the fp16 bits of the block scale selected by ``hi_mask``.
+    """
     codes, s16, _ = codec.encode(x_raw)
     c = codes.astype(np.float64) - 3.5
     s = np.repeat(s16.astype(np.float64), 32, axis=-1)
-    s_hi = np.repeat((s16.view(np.uint16) & np.uint16(0xFFE0)).view(np.float16).astype(np.float64), 32, axis=-1)
+    s_hi = np.repeat((s16.view(np.uint16) & np.uint16(hi_mask)).view(np.float16).astype(np.float64), 32, axis=-1)
     return c * s, c * s_hi, c * (s - s_hi)
 
 
 class Case:
     """One (layer, kv head) of a workload's first slot: raw Q rows of the group, K, V."""
 
-    def __init__(self, wkey: int, layer: int, g: int, n_ctx: int, T: int):
-        w = qi.WORKLOADS[wkey]
+    def __init__(self, wkey, layer: int, g: int, n_ctx: int, T: int):
+        w = qi.WORKLOADS[wkey] if isinstance(wkey, int) else wkey
         L = n_ctx + T
         self.k_raw = qi.kv_rows(w, 0, layer, g, 0, 0, L)
         self.v_raw = qi.kv_rows(w, 0, layer, g, 1, 0, L)
@@ -107,8 +117,9 @@ def _softmax_pv(s, masked, v_parts, p_mode):
 
 def ladder_q3(case: Case) -> dict:
     """Error of every scheme on the 3-bit cache (rotated basis in, unrotated out)."""
-    kv, khi, klo = exact_split_q3(case.k_raw)
-    vv, vhi, vlo = exact_split_q3(case.v_raw)
+    kv, khi, klo = exact_split_q3(case.k_raw, K_HI_MASK)
+    _, khi6, klo6 = exact_split_q3(case.k_raw, V_HI_MASK)
+    vv, vhi, vlo = exact_split_q3(case.v_raw, V_HI_MASK)
     q = rotate_f64(case.q_raw) / 16.0 * LOG2E
     qhi, qlo = split16(q)
     V = {"exact": vv, "single": f16(vv), "hi": vhi, "lo": vlo}
@@ -121,6 +132,8 @@ def ladder_q3(case: Case) -> dict:
         "p_f16": lambda: _softmax_pv(q @ kv.T, case.masked, Vexact, "f16"),
         "v_f16": lambda: _softmax_pv(q @ kv.T, case.masked, {"exact": f16(vv)}, "exact"),
         "kernel_q3": lambda: _softmax_pv(qhi @ khi.T + qlo @ khi.T + qhi @ klo.T, case.masked, V, "split"),
+        # the same with K split at 6 significant bits, as V is
+        "kernel_q3_k6": lambda: _softmax_pv(qhi @ khi6.T + qlo @ khi6.T + qhi @ klo6.T, case.masked, V, "split"),
         # the same with the fourth product Qlo.Klo: what dropping it costs
         "q3_4prod": lambda: _softmax_pv((qhi + qlo) @ kv.T, case.masked, V, "split"),
     }

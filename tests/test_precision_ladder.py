@@ -37,9 +37,28 @@ def test_ladder_reference_is_the_oracle():
 
 def test_exact_split_is_exact_in_fp16():
     x = _case().k_raw[:300]
-    val, hi, lo = pl.exact_split_q3(x)
-    assert np.array_equal(hi + lo, val)
-    assert np.array_equal(pl.f16(hi), hi) and np.array_equal(pl.f16(lo), lo)
+    for mask in (pl.K_HI_MASK, pl.V_HI_MASK):
+        val, hi, lo = pl.exact_split_q3(x, mask)
+        assert np.array_equal(hi + lo, val)
+        assert np.array_equal(pl.f16(hi), hi) and np.array_equal(pl.f16(lo), lo)
+
+
+def test_outlier_heavy_queries_and_keys_need_the_8_bit_key_split():
+    """Queries and cache both with 10x channels: scores reach ~100 (log2 units).
+
+    The dropped Qlo.Klo product with a 6-bit key split then costs more than
+    half the tolerance; with the 8-bit split it stays far inside it.
+    """
+    import q3kv_inputs as qi
+    base = qi.WORKLOADS[1]
+    w = qi.Workload(base.key, "small", 17, 1, 2, (0, 0), (0, 0), 1, "bf16", "loguniform10", "loguniform10")
+    worst6 = worst8 = 0.0
+    for g in range(2):
+        err = pl.errors(pl.ladder_q3(pl.Case(w, 0, g, 0, 300)))
+        worst6 = max(worst6, err["kernel_q3_k6"][0])
+        worst8 = max(worst8, err["kernel_q3"][0])
+    assert worst6 > MAX_ABS / 2, worst6
+    assert worst8 < MAX_ABS / 4, worst8
 
 
 def test_single_fp16_operands_miss_and_the_split_schemes_meet_the_tolerance():
