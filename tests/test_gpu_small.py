@@ -84,6 +84,24 @@ def test_ragged_slots_with_splits(impl, dtype, dist):
 
 
 @pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("split", [0, 256])
+def test_outlier_heavy_queries_and_cache_verify_shapes(impl, split):
+    """Verify widths 6..16 over 4K+ positions; queries and cache both with 10x channels."""
+    _impl_or_skip(impl)
+    w = _small("bf16", "loguniform10", slots=3)
+    ctx, T = [4096, 6000, 4500], [6, 11, 16]
+    L = [n + t for n, t in zip(ctx, T)]
+    c = GpuCache(w, L, num_layers=1)
+    kvs = [slot_kv(w, b, 0, 0, L[b]) for b in range(3)]
+    c.append_rows(0, [0, 1, 2], [0, 0, 0], kvs)
+    qs = [qi.q_rows(w, b, 0, 0, T[b]) for b in range(3)]
+    want = np.concatenate([oracle_verify(w, b, 0, ctx[b], qs[b], *kvs[b]) for b in range(3)])
+    out = c.verify(0, L, T, qs, impl=impl, split_positions=split)
+    check_close(out, want)
+    assert int(c.status.item()) == 0
+
+
+@pytest.mark.parametrize("impl", IMPLS)
 def test_batched_equals_solo_bitwise(impl):
     _impl_or_skip(impl)
     w = _small("bf16", "loguniform10", slots=3)
@@ -196,3 +214,46 @@ def test_empty_calls():
     q = qi.q_rows(w, 1, 0, 0, 1)
     out = c.verify(0, [0, 10], [0, 1], [np.zeros((0, 16, 256), np.float32), q], impl=1)
     check_close(out, oracle_verify(w, 1, 0, 9, q, k, v))
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_merge_beyond_preloaded_split_rows(impl):
+    """256-position splits over ~30K positions: 120 splits per unit (the merge preloads 96)."""
+    _impl_or_skip(impl)
+    w = _small("bf16", "loguniform10", slots=1)
+    N, T = 30_700, 3
+    c = GpuCache(w, [N + T], num_layers=1)
+    k, v = slot_kv(w, 0, 0, 0, N + T)
+    c.append_rows(0, [0], [0], [(k, v)])
+    q = qi.q_rows(w, 0, 0, 0, T)
+    out = c.verify(0, [N + T], [T], [q], impl=impl, split_positions=256)
+    check_close(out, oracle_verify(w, 0, 0, N, q, k, v))
+    assert int(c.status.item()) == 0
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_merge_beyond_one_weight_chunk(impl):
+    """2,050 splits of 256 positions (the merge stages 2,048 split weights at a time).
+
+    Every page holds the same 256 K/V vectors and the context is a whole number
+    of pages, so each position's weight appears 2,050 times and the attention
+    equals that of the single page (the oracle over one page).
+    """
+    _impl_or_skip(impl)
+    from speculative_verify_attention_q3kv_gb300 import api
+    w = qi.Workload(1, "repeat", 13, 1, 1, (0, 0), (0, 0), 1, "bf16", "outlier8", "outlier8",
+                    num_kv_heads=1, num_q_heads=8)
+    pages = 2050
+    L, T = pages * 256, 1
+    c = GpuCache(w, [L], num_layers=1)
+    k1, v1 = slot_kv(w, 0, 0, 0, 256)
+    dt = torch.bfloat16
+    kd = torch.from_numpy(k1).to(dt).cuda().repeat(pages, 1, 1)
+    vd = torch.from_numpy(v1).to(dt).cuda().repeat(pages, 1, 1)
+    zero = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.append(c.desc, c.pool, c.page_table, zero, torch.tensor([L], dtype=torch.int32).cuda(),
+               torch.tensor([0, L], dtype=torch.int32).cuda(), L, 0, kd, vd, c.status)
+    q = qi.q_rows(w, 0, 0, 0, T)
+    out = c.verify(0, [L], [T], [q], impl=impl, split_positions=256)
+    check_close(out, oracle_verify(w, 0, 0, 256 - T, q, k1, v1))
+    assert int(c.status.item()) == 0
