@@ -213,7 +213,10 @@ Q3KV_API int q3kv_verify_attn(void* stream, const q3kv_cache_desc* desc, const v
  *     nothing.
  *   - The first call on a device looks up the array's device address for that
  *     device (cudaGetSymbolAddress, with that device current) and caches it;
- *     make that first call before any stream capture.
+ *     make that first call before any stream capture.  The cached address is
+ *     kept for the life of the process: do not use this call on a device
+ *     after cudaDeviceReset, which may reload the library's device memory at
+ *     another address.
  *   - All calls share the one array: calls that overlap on the GPU (other
  *     streams, other host threads) race and may return wrong results.  The
  *     array keeps the last call's contents; the call needs no initial
