@@ -66,9 +66,9 @@ extern "C" {
 #define Q3KV_STATUS_BAD_PAGE         4
 #define Q3KV_STATUS_BAD_LENGTH       8
 #define Q3KV_STATUS_TIMEOUT         16   /* a bounded wait inside a kernel gave up */
-#define Q3KV_STATUS_RANGE           32   /* tensor-core leg: a block scale above 5696
+#define Q3KV_STATUS_RANGE           32   /* tensor-core leg: a block scale above 5458
                                             (its exact fp16 dequantisation needs
-                                            11.5 s in fp16 range) */
+                                            12 s in fp16 range) */
 
 /* input dtypes */
 #define Q3KV_F32   0
@@ -78,7 +78,7 @@ extern "C" {
 #define Q3KV_IMPL_AUTO  0   /* the fastest one that supports the shape          */
 #define Q3KV_IMPL_FMA   1   /* CUDA-core fp32 FMA flash-decode (reference leg)   */
 #define Q3KV_IMPL_MMA   2   /* tcgen05 tensor-core leg (fp16 hi/lo operand pairs,
-                               fp32 accumulation); needs block scales <= 5696   */
+                               fp32 accumulation); needs block scales <= 5458   */
 
 /* Shape of one cache pool.  Supported: head_dim 256, page_size 256,
  * num_q_heads = 8 * num_kv_heads (GQA group of 8), num_kv_heads >= 1. */

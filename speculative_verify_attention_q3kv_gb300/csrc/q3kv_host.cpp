@@ -50,14 +50,25 @@ struct Plan {
     int row_chunks;
     int split_pages;
     int num_splits;
+    int split_auto;
+    int split_target;
     size_t part_o_bytes;
     size_t part_ml_bytes;
     size_t q_prep_bytes;
     size_t total() const { return part_o_bytes + part_ml_bytes + q_prep_bytes; }
 };
 
-// Split-K policy: enough (slot, kv head, row chunk, split) CTAs to cover the
-// GPU about twice over, splits a whole number of pages.
+// Split-K policy.  A caller-fixed split size (split_positions) is used as
+// given.  Otherwise, when the (slot, kv head, row chunk) units alone do not
+// fill the GPU (tensor-core leg: one CTA per SM; CUDA-core leg: about two),
+// the kernels size the splits from the slots' own lengths (split_pages_of).
+// The host only knows the longest context and the slot count, so it sizes
+// the grid and the workspace for up to twice an even share of the target
+// CTAs per unit (and no more splits than the longest context has pages); the
+// kernels never split a slot more finely than that.  A single slot (whose
+// length is the longest), more than 32 slots, or units that fill the GPU on
+// their own (many slots, long prefills) take the split size from the longest
+// context on the host instead, an even share of the target CTAs per unit.
 int make_plan(const q3kv_cache_desc* d, int32_t num_slots, int64_t max_ctx, int32_t max_n_q, int32_t impl,
               int32_t split_positions, Plan* p, int32_t max_tokens = kMaxNq) {
     if (num_slots < 0 || max_ctx < 0 || max_n_q < 0 || max_n_q > max_tokens) return Q3KV_ERR_INVALID_ARG;
@@ -70,20 +81,30 @@ int make_plan(const q3kv_cache_desc* d, int32_t num_slots, int64_t max_ctx, int3
     const int rows = kGroup * std::max<int32_t>(max_n_q, 1);
     p->row_chunks = (rows + p->rows_per_chunk - 1) / p->rows_per_chunk;
     const int64_t pages = std::max<int64_t>(1, (max_ctx + kPageSize - 1) / kPageSize);
+    p->split_auto = 0;
+    p->split_target = 0;
     if (split_positions > 0) {
         p->split_pages = split_positions / kPageSize;
+        p->num_splits = (int)((pages + p->split_pages - 1) / p->split_pages);
     } else {
         int sms = 0;
         int e = device_sm_count(&sms);
         if (e != Q3KV_OK) return e;
-        const int64_t units = std::max<int64_t>(1, (int64_t)num_slots * d->num_kv_heads * p->row_chunks);
-        // FMA leg: about two CTAs per SM.  Tensor-core leg (one CTA per SM, a
-        // pipeline that takes a few tiles to fill): one wave.
-        const int64_t target_ctas = (impl == Q3KV_IMPL_MMA) ? (int64_t)sms : 2 * (int64_t)sms;
-        const int64_t target_splits = std::max<int64_t>(1, target_ctas / units);
-        p->split_pages = (int)std::max<int64_t>(1, (pages + target_splits - 1) / target_splits);
+        const int64_t target = (impl == Q3KV_IMPL_MMA) ? (int64_t)sms : 2 * (int64_t)sms;
+        const int64_t units_max = (int64_t)std::max(num_slots, 1) * d->num_kv_heads * p->row_chunks;
+        if (num_slots <= 1 || num_slots > 32 || units_max >= target) {
+            // one slot (its length is the longest), many slots, or units that fill the
+            // GPU alone: splits from the longest context, sized on the host
+            const int64_t ts = std::max<int64_t>(1, target / units_max);
+            p->split_pages = (int)((pages + ts - 1) / ts);
+            p->num_splits = (int)((pages + p->split_pages - 1) / p->split_pages);
+        } else {
+            p->split_auto = 1;
+            p->split_target = (int)std::max<int64_t>(1, target / d->num_kv_heads);
+            p->split_pages = 0;
+            p->num_splits = (int)std::min<int64_t>(pages, (2 * target + units_max - 1) / units_max);
+        }
     }
-    p->num_splits = (int)((pages + p->split_pages - 1) / p->split_pages);
     const int64_t units = (int64_t)std::max(num_slots, 1) * d->num_kv_heads * p->row_chunks;
     p->part_o_bytes = (size_t)(units * p->num_splits * p->rows_per_chunk * kHeadDim) * sizeof(float);
     p->part_ml_bytes = (size_t)(units * p->num_splits * p->rows_per_chunk * 2) * sizeof(float);
@@ -259,7 +280,7 @@ int verify_impl(int fmt, void* stream, const q3kv_cache_desc* desc, const void* 
     e = make_plan(desc, num_slots, max_ctx_len, max_n_q, impl, split_positions, &p, max_tokens);
     if (e != Q3KV_OK) return e;
     if (num_slots == 0 || max_n_q == 0 || max_ctx_len == 0) return Q3KV_OK;
-    if ((int64_t)desc->num_kv_heads * p.row_chunks > 65535) return Q3KV_ERR_UNSUPPORTED;   // grid.y
+    if ((int64_t)num_slots * desc->num_kv_heads * p.row_chunks > INT32_MAX) return Q3KV_ERR_UNSUPPORTED;   // grid.x
     if (!d_pool || !d_page_table || !d_ctx_len || !d_n_q || !d_q_offsets || !q || !out) return Q3KV_ERR_INVALID_ARG;
     if (!aligned16(d_pool) || !aligned16(q) || !aligned16(out)) return Q3KV_ERR_INVALID_ARG;
     if (workspace_bytes < p.total() || (p.total() > 0 && !d_workspace)) return Q3KV_ERR_WORKSPACE_TOO_SMALL;
@@ -287,6 +308,8 @@ int verify_impl(int fmt, void* stream, const q3kv_cache_desc* desc, const void* 
     a.max_n_q = max_n_q;
     a.split_pages = p.split_pages;
     a.num_splits = p.num_splits;
+    a.split_auto = p.split_auto;
+    a.split_target = p.split_target;
     a.row_chunks = p.row_chunks;
     uint8_t* ws = static_cast<uint8_t*>(d_workspace);
     a.part_o = p.part_o_bytes ? reinterpret_cast<float*>(ws) : nullptr;

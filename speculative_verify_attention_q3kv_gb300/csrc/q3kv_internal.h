@@ -72,8 +72,10 @@ struct VerifyArgs {
     int32_t dtype;
     float* out;
     int32_t max_n_q;
-    int32_t split_pages;       // pages per split-K unit
-    int32_t num_splits;        // splits of the longest slot
+    int32_t split_pages;       // pages per split-K unit (a fixed size; unused when split_auto)
+    int32_t num_splits;        // split slots per unit in the grid and the workspace (an upper bound)
+    int32_t split_auto;        // 1: the kernels size splits from the slots' own lengths (split_pages_of)
+    int32_t split_target;      // automatic policy: (slot, row chunk, split) CTAs per kv head to aim for
     int32_t row_chunks;        // CTAs along the query rows of one kv head
     float* part_o;             // [slots, kv_heads, row_chunks, splits, rows_per_chunk, 256]
     float* part_ml;            // [slots, kv_heads, row_chunks, splits, rows_per_chunk, 2]

@@ -64,7 +64,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(VerifyArgs a, int 
     const int Rc = min(rows_per_chunk, kGroup * T - row0);
     if (r >= Rc) return;
     const int n_pages = (L + kPageSize - 1) / kPageSize;
-    const int n_splits = (n_pages + a.split_pages - 1) / a.split_pages;
+    const int split_pages = split_pages_of(a);
+    const int n_splits = (n_pages + split_pages - 1) / split_pages;
     if (n_splits <= 1 || n_splits > a.num_splits) return;   // single split: the verify kernel wrote the row
 
     const float2* pml = reinterpret_cast<const float2*>(a.part_ml) + ((int64_t)unit * a.num_splits * rows_per_chunk + r);

@@ -82,10 +82,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_fma_kernel(VerifyArgs a) {
     const int lane = tid & 31;
     const int warp = tid >> 5;
 
-    const int slot = blockIdx.z;
-    const int g = blockIdx.y / a.row_chunks;
-    const int chunk = blockIdx.y % a.row_chunks;
-    const int split = blockIdx.x;
+    // units run fastest in the grid (see the tensor-core leg)
+    const int unit_id = blockIdx.x;
+    const int split = blockIdx.y;
+    const int chunk = unit_id % a.row_chunks;
+    const int g = (unit_id / a.row_chunks) % a.num_kv_heads;
+    const int slot = unit_id / (a.row_chunks * a.num_kv_heads);
 
     const int T = a.n_q[slot];
     const int L = a.ctx_len[slot];
@@ -99,14 +101,15 @@ __global__ void __launch_bounds__(kThreads, 1) verify_fma_kernel(VerifyArgs a) {
     const int Rc = min(kFmaRows, R - row0);
     if (Rc <= 0) return;
     const int n_pages = (L + kPageSize - 1) / kPageSize;
-    const int n_splits = (n_pages + a.split_pages - 1) / a.split_pages;
+    const int split_pages = split_pages_of(a);
+    const int n_splits = (n_pages + split_pages - 1) / split_pages;
     if (n_splits > a.num_splits) {   // context longer than the host bound the workspace was sized for
         if (tid == 0 && split == 0 && chunk == 0 && g == 0 && a.status) atomicOr(a.status, Q3KV_STATUS_BAD_LENGTH);
         return;
     }
     if (split >= n_splits) return;
-    const int p_begin = split * a.split_pages * kPageSize;
-    const int p_end = min(L, p_begin + a.split_pages * kPageSize);
+    const int p_begin = split * split_pages * kPageSize;
+    const int p_end = min(L, p_begin + split_pages * kPageSize);
     const int N = L - T;
     const int Hq = a.num_kv_heads * kGroup;
     const int64_t q_base = a.q_offsets[slot];
@@ -294,7 +297,7 @@ namespace {
 template <typename TIn, int FMT>
 cudaError_t launch_fma_typed(const VerifyArgs& a, cudaStream_t stream) {
     const size_t smem = sizeof(FmaSmem);
-    const dim3 grid((unsigned)a.num_splits, (unsigned)(a.num_kv_heads * a.row_chunks), (unsigned)a.num_slots);
+    const dim3 grid((unsigned)(a.num_slots * a.num_kv_heads * a.row_chunks), (unsigned)a.num_splits);
     const cudaError_t e =
         cudaFuncSetAttribute(verify_fma_kernel<TIn, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

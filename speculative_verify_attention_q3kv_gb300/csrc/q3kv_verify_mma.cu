@@ -16,12 +16,12 @@
 // single fp16 operand per side misses by 10-20x on outlier-heavy caches.  So
 // every operand is carried as an exact or near-exact fp16 pair:
 //   K_hat = (c - 3.5) s = (c - 3.5) s_hi + (c - 3.5) s_lo, with s_hi = s rounded
-//           down to 8 significant bits; both products are exact in fp16;
-//   V_hat likewise with a 6-bit s_hi (then each half is one fused multiply-add
-//   from the code); Q = Q_hi + Q_lo and P = P_hi + P_lo (round-to-nearest
+//           down to 8 significant bits; both products are exact in fp16 and
+//           each is one fused multiply-add from the code;
+//   V_hat likewise; Q = Q_hi + Q_lo and P = P_hi + P_lo (round-to-nearest
 //   splits); each contraction sums the three leading products
 //   (hi.hi + hi.lo + lo.hi) with fp32 accumulation in TMEM.  The dropped
-//   lo.lo product is below 2^-20 of the scores (K) and 2^-17 of P.V_hat.
+//   lo.lo products are below 2^-20 of the scores and of P.V_hat.
 // The fp8 format (template FMT = kFmtFp8) decodes K and V exactly into single
 // fp16 values (one conversion per pair), so each contraction has two products
 // (K.Q_hi + K.Q_lo, V.P_hi + V.P_lo); it is not rotated, so the query kernel
@@ -119,7 +119,7 @@ constexpr long long kWaitCycles = 2000000000LL;
 // A waiting thread is suspended (not spinning) until the phase completes or
 // this many nanoseconds pass, so idle warps leave the issue slots to the others.
 constexpr uint32_t kSuspendHintNs = 100000;
-constexpr float kMaxScale = 5696.0f;        // 11.5 * s must stay below the fp16 maximum
+constexpr float kMaxScale = 5458.0f;        // 12 * s must stay below the fp16 maximum
 
 // TMEM columns (allocation of 512)
 constexpr uint32_t kColKHi = 0;
@@ -375,17 +375,18 @@ constexpr uint32_t kVLbo = 128, kVSbo = 2 * 128;
 constexpr uint32_t kPLbo = 128, kPSbo = 16 * 128;
 
 // ---------------------------------------------------------------- dequantisation
-// fp16 pair (8 + c_even, 8 + c_odd) from two 3-bit fields at bit offsets off
-// and off + 16: 0x4800 is 8 with ulp 1/128, so a code goes in at bit 7.
+// fp16 pair (8.5 + c_even, 8.5 + c_odd) from two 3-bit fields at bit offsets
+// off and off + 16: 0x4800 is 8 with ulp 1/128, so a code goes in at bit 7,
+// and 0x0040 adds the half (exact: 8.5 + c has at most 5 significant bits).
 __device__ __forceinline__ uint32_t code_pair_word(uint32_t w, int off) {
     const uint32_t x = (off >= 7) ? (w >> (off - 7)) : (w << (7 - off));
-    return (x & 0x03800380u) | 0x48004800u;
+    return (x & 0x03800380u) | 0x48404840u;
 }
 __device__ __forceinline__ uint32_t code_pair_last(uint32_t w0, uint32_t w1, uint32_t w2) {
     // element 30: bit 15 of w0, w1, w2 -> code bits 0,1,2 (into fp16 mantissa bits 7,8,9)
     // element 31: bit 31 of w0, w1, w2
     const uint32_t x = ((w0 >> 8) & 0x00800080u) | ((w1 >> 7) & 0x01000100u) | ((w2 >> 6) & 0x02000200u);
-    return x | 0x48004800u;
+    return x | 0x48404840u;
 }
 
 __device__ __forceinline__ __half2 as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
@@ -403,18 +404,22 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& p01, uint32_
 }
 
 // One 32-element block: 16 pairs of (c - 3.5) s_hi and (c - 3.5) s_lo, where
-// s_hi keeps the top 6 significant bits of s and s_lo = s - s_hi the other 5.
-// With x = 8 + c, (c - 3.5) s_part = x s_part - 11.5 s_part: the constant
-// 11.5 s_part (5 + 6 bits) and the result (3 + 6 or 3 + 5 bits) are exact in
-// fp16, so one fused multiply-add per half gives each product exactly (for
-// s <= 65504 / 11.5 = 5696; larger scales are flagged).
+// s_hi keeps the top 8 significant bits of s and s_lo = s - s_hi the other 3.
+// With x = 8.5 + c, (c - 3.5) s_part = x s_part - 12 s_part: the constant
+// 12 s_part (2 + 8 or 2 + 3 bits) and the result (3 + 8 or 3 + 3 bits) are
+// exact in fp16, so one fused multiply-add per half gives each product
+// exactly, for s <= 65504 / 12 (larger scales are flagged).  With 8 bits in
+// s_hi the products the three-product contractions drop, Q_lo . K_hat_lo and
+// P_lo . V_hat_lo, are below 2^-20 of the scores and of P . V_hat (a 6-bit
+// s_hi left Q_lo . K_hat_lo at 2^-18, which at scores near 100 in log2 units,
+// with outlier-heavy queries and keys, alone cost up to 2e-3 of output).
 __device__ __forceinline__ void dequant_block(const uint32_t* w3, __half s, uint32_t (&hi)[16], uint32_t (&lo)[16]) {
-    const __half s_hi = __ushort_as_half((unsigned short)(__half_as_ushort(s) & 0xFFE0u));
+    const __half s_hi = __ushort_as_half((unsigned short)(__half_as_ushort(s) & 0xFFF8u));
     const __half s_lo = __hsub(s, s_hi);
-    const __half m115 = __ushort_as_half((unsigned short)0xC9C0u);   // -11.5
+    const __half m12 = __ushort_as_half((unsigned short)0xCA00u);   // -12
     const __half2 sh2 = __halves2half2(s_hi, s_hi);
     const __half2 sl2 = __halves2half2(s_lo, s_lo);
-    const __half ch = __hmul(s_hi, m115), cl = __hmul(s_lo, m115);
+    const __half ch = __hmul(s_hi, m12), cl = __hmul(s_lo, m12);
     const __half2 ch2 = __halves2half2(ch, ch);
     const __half2 cl2 = __halves2half2(cl, cl);
     const uint32_t w0 = w3[0], w1 = w3[1], w2 = w3[2];
@@ -429,34 +434,6 @@ __device__ __forceinline__ void dequant_block(const uint32_t* w3, __half s, uint
         }
         hi[m] = as_u32(__hfma2(as_h2(x), sh2, ch2));     // (c - 3.5) s_hi, exact
         lo[m] = as_u32(__hfma2(as_h2(x), sl2, cl2));     // (c - 3.5) s_lo, exact
-    }
-}
-
-// K_hat blocks are split with 8 significant bits in s_hi (s_lo keeps the
-// other 3): the product Q_lo . K_hat_lo, which the three-product contraction
-// drops, is then below 2^-20 of |Q . K_hat| (with a 6-bit s_hi it reached
-// 2^-18, and at scores of ~100 in log2 units with outlier-heavy queries and
-// keys that alone cost up to 2e-3 of output).  c - 3.5 = (8 + c) - 11.5 is
-// exact, and so are (c - 3.5) s_hi (3 + 8 bits) and (c - 3.5) s_lo (3 + 3).
-__device__ __forceinline__ void dequant_block_k(const uint32_t* w3, __half s, uint32_t (&hi)[16], uint32_t (&lo)[16]) {
-    const __half s_hi = __ushort_as_half((unsigned short)(__half_as_ushort(s) & 0xFFF8u));
-    const __half s_lo = __hsub(s, s_hi);
-    const __half2 sh2 = __halves2half2(s_hi, s_hi);
-    const __half2 sl2 = __halves2half2(s_lo, s_lo);
-    const __half2 m115 = as_h2(0xC9C0C9C0u);   // (-11.5, -11.5)
-    const uint32_t w0 = w3[0], w1 = w3[1], w2 = w3[2];
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        uint32_t x;
-        if (m < 15) {
-            const uint32_t w = (m < 5) ? w0 : (m < 10 ? w1 : w2);
-            x = code_pair_word(w, 3 * (m % 5));
-        } else {
-            x = code_pair_last(w0, w1, w2);
-        }
-        const __half2 c = __hadd2(as_h2(x), m115);       // c - 3.5, exact
-        hi[m] = as_u32(__hmul2(c, sh2));
-        lo[m] = as_u32(__hmul2(c, sl2));
     }
 }
 
@@ -610,10 +587,13 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
     const int lane = tid & 31;
     const int warp = tid >> 5;
 
-    const int slot = blockIdx.z;
-    const int g = blockIdx.y / a.row_chunks;
-    const int chunk = blockIdx.y % a.row_chunks;
-    const int split = blockIdx.x;
+    // units run fastest in the grid, so every unit's first splits are
+    // dispatched before any unit's later ones (most of which exit at once)
+    const int unit_id = blockIdx.x;
+    const int split = blockIdx.y;
+    const int chunk = unit_id % a.row_chunks;
+    const int g = (unit_id / a.row_chunks) % a.num_kv_heads;
+    const int slot = unit_id / (a.row_chunks * a.num_kv_heads);
 
     const int T = a.n_q[slot];
     const int L = a.ctx_len[slot];
@@ -627,19 +607,20 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
     const int Rc = min(kRows, R - row0);
     if (Rc <= 0) return;
     const int n_pages = (L + kPageSize - 1) / kPageSize;
-    const int n_splits = (n_pages + a.split_pages - 1) / a.split_pages;
+    const int split_pages = split_pages_of(a);
+    const int n_splits = (n_pages + split_pages - 1) / split_pages;
     if (n_splits > a.num_splits) {
         if (tid == 0 && split == 0 && chunk == 0 && g == 0 && a.status) atomicOr(a.status, Q3KV_STATUS_BAD_LENGTH);
         return;
     }
     if (split >= n_splits) return;
-    const int p_begin = split * a.split_pages * kPageSize;
+    const int p_begin = split * split_pages * kPageSize;
     const int Nctx = L - T;
     // positions past the causal limit of this CTA's last row are masked for all
     // of its rows, so they are not read (long prefills: later rows see more);
     // at least one position is kept so every CTA of a split writes its partial
     const int p_vis = Nctx + (row0 + Rc - 1) / kGroup + 1;
-    const int p_end = min(min(L, p_begin + a.split_pages * kPageSize), max(p_vis, p_begin + 1));
+    const int p_end = min(min(L, p_begin + split_pages * kPageSize), max(p_vis, p_begin + 1));
     const int n_tiles = (p_end - p_begin + kTileP - 1) / kTileP;
     const int Hq = a.num_kv_heads * kGroup;
     const int64_t q_base = a.q_offsets[slot];
@@ -1001,7 +982,7 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                     for (int bb = 0; bb < 4; ++bb) {
                         uint32_t hi[16], lo[16];
                         const __half s = __ushort_as_half((unsigned short)((bb & 1) ? (sh[bb >> 1] >> 16) : (sh[bb >> 1] & 0xFFFFu)));
-                        dequant_block_k(&wh[3 * bb], s, hi, lo);
+                        dequant_block(&wh[3 * bb], s, hi, lo);
                         range_bad |= valid && !(__half2float(s) <= kMaxScale);
                         tmem_st16(col + kColKHi + 16 * bb, hi);
                         tmem_st16(col + kColKLo + 16 * bb, lo);
@@ -1226,7 +1207,7 @@ cudaError_t launch_typed(const VerifyArgs& a, cudaStream_t stream, std::atomic<b
     // the verify grid may start while the query kernel runs: only its QK
     // issuer waits (griddepcontrol.wait) for the queries
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.num_splits, (unsigned)(a.num_kv_heads * a.row_chunks), (unsigned)a.num_slots);
+    cfg.gridDim = dim3(units, (unsigned)a.num_splits);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;

@@ -16,8 +16,8 @@ The tensor-core leg's own choices, as emulated by ``kernel_q3`` and
 * Q is rotated and scaled into log2 units (H q / 16 * log2 e), then split into
   round-to-nearest fp16 hi/lo;
 * the 3-bit K/V values (c - 3.5) s are split exactly: s_hi = s with its fp16
-  mantissa cut to 8 (K) or 6 (V) significant bits, s_lo = s - s_hi, so
-  (c - 3.5) s_hi and (c - 3.5) s_lo are both exact in fp16;
+  mantissa cut to 8 significant bits, s_lo = s - s_hi, so (c - 3.5) s_hi and
+  (c - 3.5) s_lo are both exact in fp16;
 * S = Qhi.Khi + Qlo.Khi + Qhi.Klo (the Qlo.Klo product is dropped: below
   2^-20 of the scores with the 8-bit K split; a 6-bit K split left it at
   2^-18, which on outlier-heavy queries and keys costs up to 2e-3 of output,
@@ -62,8 +62,9 @@ def split16(x):
     return hi, f16(np.asarray(x, np.float64) - hi)
 
 
-K_HI_MASK = 0xFFF8   # fp16 bits of s kept in s_hi for K: 8 significant bits
-V_HI_MASK = 0xFFE0   # for V: 6 significant bits
+K_HI_MASK = 0xFFF8   # fp16 bits of s kept in s_hi: 8 significant bits (K and V)
+V_HI_MASK = K_HI_MASK
+K6_HI_MASK = 0xFFE0  # 6 significant bits: the earlier key split, kept as a ladder row
 
 
 def exact_split_q3(x_raw, hi_mask=V_HI_MASK):
@@ -118,7 +119,7 @@ def _softmax_pv(s, masked, v_parts, p_mode):
 def ladder_q3(case: Case) -> dict:
     """Error of every scheme on the 3-bit cache (rotated basis in, unrotated out)."""
     kv, khi, klo = exact_split_q3(case.k_raw, K_HI_MASK)
-    _, khi6, klo6 = exact_split_q3(case.k_raw, V_HI_MASK)
+    _, khi6, klo6 = exact_split_q3(case.k_raw, K6_HI_MASK)
     vv, vhi, vlo = exact_split_q3(case.v_raw, V_HI_MASK)
     q = rotate_f64(case.q_raw) / 16.0 * LOG2E
     qhi, qlo = split16(q)
@@ -132,7 +133,7 @@ def ladder_q3(case: Case) -> dict:
         "p_f16": lambda: _softmax_pv(q @ kv.T, case.masked, Vexact, "f16"),
         "v_f16": lambda: _softmax_pv(q @ kv.T, case.masked, {"exact": f16(vv)}, "exact"),
         "kernel_q3": lambda: _softmax_pv(qhi @ khi.T + qlo @ khi.T + qhi @ klo.T, case.masked, V, "split"),
-        # the same with K split at 6 significant bits, as V is
+        # the same with K split at 6 significant bits
         "kernel_q3_k6": lambda: _softmax_pv(qhi @ khi6.T + qlo @ khi6.T + qhi @ klo6.T, case.masked, V, "split"),
         # the same with the fourth product Qlo.Klo: what dropping it costs
         "q3_4prod": lambda: _softmax_pv((qhi + qlo) @ kv.T, case.masked, V, "split"),

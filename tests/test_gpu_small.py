@@ -202,6 +202,30 @@ def test_status_nonfinite_and_overflow():
     assert int(c.status.item()) == 2
 
 
+@pytest.mark.parametrize("scale_value,flagged", [(4.0e5, True), (1.0e5, False)])
+def test_status_range_of_the_tensor_core_leg(scale_value, flagged):
+    """A block scale above 65504 / 12 (one input channel at 4e5 rotates to 25,000 in every dim:
+    s = 7,143) is flagged by the tensor-core leg and read by the CUDA-core leg; 1e5 (s = 1,786)
+    is read by both."""
+    w = _small("f32", "outlier8", slots=1)
+    N, T = 40, 2
+    c = GpuCache(w, [N + T], num_layers=1)
+    k, v = slot_kv(w, 0, 0, 0, N + T)
+    k[5, 1, 17] = scale_value
+    c.append_rows(0, [0], [0], [(k, v)])
+    assert int(c.status.item()) == 0
+    q = qi.q_rows(w, 0, 0, 0, T)
+    want = oracle_verify(w, 0, 0, N, q, k, v)
+    check_close(c.verify(0, [N + T], [T], [q], impl=1), want)
+    assert int(c.status.item()) == 0
+    out = c.verify(0, [N + T], [T], [q], impl=2)
+    if flagged:
+        assert int(c.status.item()) & 32
+    else:
+        assert int(c.status.item()) == 0
+        check_close(out, want)
+
+
 def test_empty_calls():
     w = _small("f32", "outlier8", slots=2)
     c = GpuCache(w, [10, 10], num_layers=1)

@@ -69,3 +69,35 @@ def test_single_fp16_operands_miss_and_the_split_schemes_meet_the_tolerance():
         assert err[name][0] > MAX_ABS, (name, err[name])
     assert err["kernel_q3"][0] < MAX_ABS / 5 and err["kernel_q3"][1] < REL_L2 / 10, err["kernel_q3"]
     assert err["kernel_fp8"][0] < MAX_ABS / 20 and err["kernel_fp8"][1] < REL_L2 / 100, err["kernel_fp8"]
+
+
+def test_one_fused_multiply_add_per_half_is_exact_for_every_scale():
+    """The tensor-core leg's dequantisation, for every fp16 scale it accepts.
+
+    From x = 8.5 + c (exact in fp16), each half (c - 3.5) s_part is formed as
+    one fused multiply-add x * s_part + (-12 s_part).  It is exact when -12
+    s_part is exact in fp16 and the result is: checked exhaustively over all
+    positive fp16 scales from 2^-13 up to the leg's limit 65504 / 12, all
+    eight codes, with the fused operation's single rounding emulated in
+    float64 (the product of two fp16 numbers is exact there).  A smaller scale
+    (a block whose largest value is below 4.3e-4) can leave the lo half off by
+    at most 2^-25.
+    """
+    s16 = np.arange(1, 0x7C00, dtype=np.uint16).view(np.float16)
+    s16 = s16[s16.astype(np.float64) <= 65504.0 / 12.0]
+    s = s16.astype(np.float64)
+    s_hi16 = (s16.view(np.uint16) & np.uint16(pl.K_HI_MASK)).view(np.float16)
+    s_hi = s_hi16.astype(np.float64)
+    s_lo = s - s_hi
+    assert np.array_equal(pl.f16(s_lo), s_lo)                       # s_lo exact in fp16
+    normal = s >= 2.0 ** -13          # s_lo is then a multiple of 2^-23
+    for part in (s_hi, s_lo):
+        const = -12.0 * part
+        assert np.array_equal(pl.f16(const), const)                 # the FMA's addend is exact
+        for c in range(8):
+            fused = pl.f16((8.5 + c) * part + const)                # one rounding
+            assert np.array_equal(fused[normal], (c - 3.5) * part[normal]), c
+            assert np.abs(fused - (c - 3.5) * part).max() <= 2.0 ** -25
+    # and the pair adds up to the decoded value
+    for c in range(8):
+        assert np.array_equal((c - 3.5) * s_hi + (c - 3.5) * s_lo, (c - 3.5) * s)
