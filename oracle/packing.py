@@ -24,21 +24,6 @@ table names p at index i.  Inside the pool the record of
   ((((page * num_layers + layer) * num_kv_heads + kv_head) * 2 + kv) * 256 + r) * 112
 
 so one (page, layer, kv head) is a 28,672-byte K chunk followed by its V chunk.
-The K chunk holds the 256 records.  The V chunk ("value page") holds the same
-codes and scales arranged by dimension, so that one GPU thread per dimension
-reads the codes of many positions from one word:
-
-  bytes     0..24575 : code planes.  For tile t (positions [128t, 128t + 128) of
-                       the page) and dimension d, 12 uint32 words at word index
-                       (t * 256 + d) * 12; word 3g + j of them belongs to group g
-                       (positions [128t + 32g, 128t + 32g + 32)).  Position i of a
-                       group sits in its 3 words exactly as element i of a record
-                       block sits in the block's 3 words (pairs of positions per
-                       shift and mask, positions 30 and 31 as bit planes).
-  bytes 24576..28671 : scales.  fp16 of (position p, block b) at byte
-                       24576 + ((t * 8 + b) * 128 + p % 128) * 2, t = p // 128.
-
-Each tile's codes (12,288 bytes) and scales (2,048 bytes) are contiguous.
 """
 from __future__ import annotations
 
@@ -95,49 +80,3 @@ def record_offset(num_layers: int, num_kv_heads: int, page: int, layer: int, kv_
 
 def pool_bytes(num_pages: int, num_layers: int, num_kv_heads: int) -> int:
     return num_pages * num_layers * num_kv_heads * 2 * PAGE_SIZE * RECORD_BYTES
-
-
-# ---------------------------------------------------------------- value pages
-VALUE_TILE = 128                                  # positions per tile of a value page
-VALUE_CODE_BYTES = 2 * 256 * 12 * 4               # 24,576
-VALUE_PAGE_BYTES = VALUE_CODE_BYTES + 256 * 8 * 2  # 28,672: the size of 256 records
-
-
-def value_code_word(position: int, dim: int, j: int) -> int:
-    """Index (in uint32 words from the page's start) of word j of (position's group, dim)."""
-    t, r = divmod(position, VALUE_TILE)
-    return (t * 256 + dim) * 12 + 3 * (r // 32) + j
-
-
-def value_scale_byte(position: int, block: int) -> int:
-    t, r = divmod(position, VALUE_TILE)
-    return VALUE_CODE_BYTES + ((t * 8 + block) * VALUE_TILE + r) * 2
-
-
-def pack_value_page(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
-    """codes uint8 [256 positions, 256 dims], scales float16 [256, 8] -> uint8 [28672]."""
-    c = np.asarray(codes, dtype=np.uint32).reshape(2, 4, 32, 256)       # [tile, group, i, dim]
-    words = np.zeros((2, 256, 4, 3), dtype=np.uint32)                     # [tile, dim, group, j]
-    for i in range(32):
-        ci = np.transpose(c[:, :, i, :], (0, 2, 1))                       # [tile, dim, group]
-        for wi, bit, k in _field(i):
-            words[..., wi] |= ((ci >> np.uint32(k)) & np.uint32(1)) << np.uint32(bit)
-    out = np.empty(VALUE_PAGE_BYTES, dtype=np.uint8)
-    out[:VALUE_CODE_BYTES] = words.astype("<u4").reshape(-1).view(np.uint8)
-    sc = np.asarray(scales, dtype="<f2").reshape(2, 128, 8).transpose(0, 2, 1)   # [tile, block, row]
-    out[VALUE_CODE_BYTES:] = np.ascontiguousarray(sc).reshape(-1).view(np.uint8)
-    return out
-
-
-def unpack_value_page(page: np.ndarray):
-    """uint8 [28672] -> (codes uint8 [256 positions, 256 dims], scales float16 [256, 8])."""
-    page = np.ascontiguousarray(page, dtype=np.uint8)
-    words = page[:VALUE_CODE_BYTES].copy().view("<u4").reshape(2, 256, 4, 3).astype(np.uint32)
-    c = np.zeros((2, 4, 32, 256), dtype=np.uint32)
-    for i in range(32):
-        acc = np.zeros((2, 256, 4), dtype=np.uint32)
-        for wi, bit, k in _field(i):
-            acc |= ((words[..., wi] >> np.uint32(bit)) & np.uint32(1)) << np.uint32(k)
-        c[:, :, i, :] = np.transpose(acc, (0, 2, 1))
-    sc = page[VALUE_CODE_BYTES:].copy().view("<f2").reshape(2, 8, 128).transpose(0, 2, 1)
-    return c.reshape(256, 256).astype(np.uint8), np.ascontiguousarray(sc).reshape(256, 8).astype(np.float16)

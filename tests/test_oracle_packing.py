@@ -78,75 +78,3 @@ def test_record_offsets():
     assert packing.record_offset(L, H, 1, 0, 0, 0, 0) == 16 * 2 * 2 * 256 * 112
     assert packing.pool_bytes(3, L, H) == 3 * 16 * 2 * 2 * 256 * 112
     assert packing.record_offset(L, H, 2, 15, 1, 1, 255) + 112 == packing.pool_bytes(3, L, H)
-
-
-# ---------------------------------------------------------------- value pages
-VGOLDEN = os.path.join(os.path.dirname(__file__), "golden", "value_page_hand_examples.json")
-
-
-def test_value_page_hand_examples():
-    for case in json.load(open(VGOLDEN))["cases"]:
-        codes = np.zeros((256, 256), np.uint8)
-        for p, d, c in case["codes"]:
-            codes[p, d] = c
-        scales = np.zeros((256, 8), np.float16)
-        for p, b, hx in case["scales"]:
-            scales[p, b] = np.frombuffer(bytes.fromhex(hx)[::-1], dtype="<f2")[0]
-        page = packing.pack_value_page(codes, scales)
-        assert page.shape == (packing.VALUE_PAGE_BYTES,) == (256 * 112,)
-        words = page[:packing.VALUE_CODE_BYTES].view("<u4")
-        want = np.zeros(words.shape, np.uint32)
-        for w, hx in case["words_hex"].items():
-            want[int(w)] = int(hx, 16)
-        assert np.array_equal(words, want), case["why"]
-        sbytes = page[packing.VALUE_CODE_BYTES:]
-        want_s = np.zeros(sbytes.shape, np.uint8)
-        for off, hx in case["scale_bytes_hex"].items():
-            o = int(off) - packing.VALUE_CODE_BYTES
-            want_s[o:o + 2] = np.frombuffer(bytes.fromhex(hx), np.uint8)
-        assert np.array_equal(sbytes, want_s), case["why"]
-        c2, s2 = packing.unpack_value_page(page)
-        assert np.array_equal(c2, codes) and np.array_equal(s2.view(np.uint16), scales.view(np.uint16))
-
-
-def test_value_page_every_bit_used_once():
-    # every (position, dim) code bit lands on its own bit of the code planes
-    seen = np.zeros(packing.VALUE_CODE_BYTES * 8, np.int32)
-    rng = np.random.default_rng(3)
-    for p in list(range(0, 256, 17)) + [30, 31, 126, 127, 128, 159, 254, 255]:
-        for d in rng.choice(256, 6, replace=False):
-            for k in range(3):
-                codes = np.zeros((256, 256), np.uint8)
-                codes[p, d] = 1 << k
-                bits = np.unpackbits(packing.pack_value_page(codes, np.zeros((256, 8), np.float16))
-                                     [:packing.VALUE_CODE_BYTES], bitorder="little")
-                assert bits.sum() == 1
-                seen[np.argmax(bits)] += 1
-    assert seen.max() == 1
-    # and the code area is exactly 256 positions x 256 dims x 3 bits
-    assert packing.VALUE_CODE_BYTES * 8 == 256 * 256 * 3
-
-
-def test_value_page_position_pairs_extract_with_shift_and_mask():
-    # the property the planes exist for: one word of a dimension gives positions (2m, 2m+1)
-    rng = np.random.default_rng(4)
-    codes = rng.integers(0, 8, (256, 256)).astype(np.uint8)
-    words = packing.pack_value_page(codes, np.zeros((256, 8), np.float16))[:packing.VALUE_CODE_BYTES].view("<u4")
-    for t in range(2):
-        for d in (0, 77, 255):
-            base = (t * 256 + d) * 12
-            for g in range(4):
-                p0 = 128 * t + 32 * g
-                for m in range(15):
-                    w = int(words[base + 3 * g + m // 5]) >> (3 * (m % 5))
-                    assert (w & 7) == codes[p0 + 2 * m, d] and ((w >> 16) & 7) == codes[p0 + 2 * m + 1, d]
-
-
-def test_value_page_holds_the_records_codes():
-    # the same codes and scales as the 112-byte records of the page's positions, rearranged
-    rng = np.random.default_rng(5)
-    codes = rng.integers(0, 8, (256, 256)).astype(np.uint8)
-    scales = rng.standard_normal((256, 8)).astype(np.float16)
-    rc, rs = packing.unpack_records(packing.pack_records(codes, scales))
-    vc, vs = packing.unpack_value_page(packing.pack_value_page(codes, scales))
-    assert np.array_equal(rc, vc) and np.array_equal(rs.view(np.uint16), vs.view(np.uint16))
