@@ -44,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 # from ncu captures of the current kernel in this benchmark's launch configuration
 # (profiles/); the roofline's traffic is this times the launch's positions.
 # Workloads without a capture of the current kernel report null.
-NCU_TRAFFIC_BYTES_PER_POSITION = {}
+NCU_TRAFFIC_BYTES_PER_POSITION = {5: 227.16, 4: 234.04, 3: 229.60, 2: 227.67}
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -518,7 +518,7 @@ def run_ours(args, rank, world, local, pg):
     if args.verify_impl == "auto" and args.kv == "q3" and args.split == 0:
         per_pos = NCU_TRAFFIC_BYTES_PER_POSITION.get(w.key)
         if per_pos is not None:
-            traffic = per_pos * kv_bytes / 224.0 / w.num_kv_heads
+            traffic = per_pos * kv_bytes / 224.0          # kv_bytes / 224 = attended (position, kv head) pairs
     ctxs = [st.ctx for st in steps]
     news = [st.n_new for st in steps]
     line = {
