@@ -66,7 +66,7 @@ def parse():
                          "attention over the 3-bit cache, every layer of the workload, one slot)")
     ap.add_argument("--kv", default="q3", choices=["q3", "fp8", "t5k"],
                     help="cache format: the 3-bit rotated codec, the fp8 E4M3 comparison format, or the "
-                         "turbo5k-style 5-bit K / 3-bit V format (CUDA-core leg)")
+                         "turbo5k-style 5-bit K / 3-bit V format")
     return ap.parse_args()
 
 
@@ -293,8 +293,6 @@ class Step:
         self.max_new = max(self.n_new)
         self.max_ctx = max(self.Ltot)
         self.impl = {"auto": 0, "fma": 1, "mma": 2}[verify_impl]
-        if cache.kv == "t5k":
-            self.impl = 1                      # the turbo5k-style cache is read by the CUDA-core leg
         self.split = split
         self.ws = ws if ws is not None else torch.zeros(
             api.workspace_bytes(cache.desc, self.S, self.max_ctx, self.max_new, self.impl, split),

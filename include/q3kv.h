@@ -298,9 +298,10 @@ Q3KV_API int q3kv_fp8_verify_attn(void* stream, const q3kv_cache_desc* desc, con
  *     ((page * L + layer) * H + head) * 70,656 + row * 164 (K), or
  *     + 41,984 + row * 112 (V).  Pages, page tables, lengths, allocator as the
  *     3-bit cache.
- *   - Verify: the CUDA-core leg (impl AUTO or FMA; MMA returns
- *     Q3KV_ERR_UNSUPPORTED); the workspace is q3kv_workspace_bytes(...) with
- *     impl Q3KV_IMPL_FMA.
+ *   - Verify: both legs (impl AUTO = the tensor-core leg, which reads K_hat =
+ *     centroid * s rounded to float32 and split into fp16 hi/lo, within 2^-22
+ *     of the exact value, and flags Q3KV_STATUS_RANGE for a K scale above
+ *     20,000); the workspace is q3kv_workspace_bytes(...) with the same impl.
  * Arguments, ownership, errors and status bits as q3kv_pool_bytes,
  * q3kv_append and q3kv_verify_attn. */
 Q3KV_API int q3kv_t5k_pool_bytes(const q3kv_cache_desc* desc, size_t* bytes);

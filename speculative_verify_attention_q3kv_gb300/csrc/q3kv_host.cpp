@@ -272,10 +272,6 @@ int verify_impl(int fmt, void* stream, const q3kv_cache_desc* desc, const void* 
     if (max_n_q > max_tokens) return Q3KV_ERR_UNSUPPORTED;
     if (impl < Q3KV_IMPL_AUTO || impl > Q3KV_IMPL_MMA) return Q3KV_ERR_INVALID_ARG;
     if (fmt == kFmtFp8 && impl == Q3KV_IMPL_FMA) return Q3KV_ERR_UNSUPPORTED;   // tensor-core leg only
-    if (fmt == kFmtT5k) {                                                       // CUDA-core leg only
-        if (impl == Q3KV_IMPL_MMA) return Q3KV_ERR_UNSUPPORTED;
-        impl = Q3KV_IMPL_FMA;
-    }
     Plan p;
     e = make_plan(desc, num_slots, max_ctx_len, max_n_q, impl, split_positions, &p, max_tokens);
     if (e != Q3KV_OK) return e;

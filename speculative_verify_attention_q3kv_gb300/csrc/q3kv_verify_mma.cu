@@ -120,6 +120,7 @@ constexpr long long kWaitCycles = 2000000000LL;
 // this many nanoseconds pass, so idle warps leave the issue slots to the others.
 constexpr uint32_t kSuspendHintNs = 100000;
 constexpr float kMaxScale = 5458.0f;        // 12 * s must stay below the fp16 maximum
+constexpr float kMaxT5kScale = 20000.0f;    // turbo5k K: the largest centroid (3.27) times s within fp16
 
 // TMEM columns (allocation of 512)
 constexpr uint32_t kColKHi = 0;
@@ -488,7 +489,7 @@ __device__ __forceinline__ int32_t tile_page(const VerifyArgs& a, const int32_t*
 // Issues the bulk copy of n records (kv 0 = K, 1 = V) of the tile at pos0,
 // starting at row r0 of the tile, or, for a page id out of range, flags it
 // and completes the phase without data (the readers zero that tile).
-template <int RECB>
+template <int FMT>
 __device__ __forceinline__ void issue_rec_copy(const VerifyArgs& a, const int32_t* pt_row, int g, int kv, int pos0,
                                                int r0, int n, uint8_t* dst, unsigned long long* full) {
     const int32_t page = pt_row[pos0 / kPageSize];
@@ -497,8 +498,11 @@ __device__ __forceinline__ void issue_rec_copy(const VerifyArgs& a, const int32_
         mbar_arrive(full);
         return;
     }
+    constexpr int RECB = Fmt<FMT>::kRecB;
     const uint8_t* src =
-        a.pool + record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, kv, pos0 % kPageSize + r0, RECB);
+        a.pool + (FMT == kFmtT5k ? t5k_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, kv, pos0 % kPageSize + r0)
+                                 : record_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, kv,
+                                                 pos0 % kPageSize + r0, RECB));
     const uint32_t bytes = (uint32_t)(n * RECB);
     fence_proxy_async();
     mbar_arrive_expect_tx(full, bytes);
@@ -669,7 +673,7 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         const int q = warp & 3;
         for (int e = 0; e < 2; ++e) {
             const int r0 = kSubP * (q + 4 * e);
-            issue_rec_copy<kRecB>(a, pt_row, g, 1, p_begin, r0, kSubP, sm.vrec + kRecB * r0, &bar.vfull[q][e]);
+            issue_rec_copy<FMT>(a, pt_row, g, 1, p_begin, r0, kSubP, sm.vrec + kRecB * r0, &bar.vfull[q][e]);
         }
     }
     if (warp == 12 && lane == 0) {
@@ -934,6 +938,71 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                     if (lane == 0) mbar_arrive(&bar.kready[hh]);
                 }
             }
+        } else if constexpr (FMT == kFmtT5k) {
+            // turbo5k K: thread p's 164-byte record, a 128-dim half at a time (64
+            // nibble bytes, 16 bytes of 5th bits, the two scales), the next half's
+            // loads in flight while this one decodes.  A code's centroid comes from
+            // a shuffle (lane l holds centroid l); K_hat = centroid * s in float32,
+            // split into round-to-nearest fp16 hi/lo (within 2^-22 of K_hat).
+            const float cent = a.t5k.c[lane];
+            auto fetch_half = [&](int i, int hh, uint32_t (&w)[21]) {
+                const int pos0 = p_begin + i * kTileP;
+                const int32_t page = (i < n_tiles) ? tile_page(a, pt_row, pos0) : -1;
+                if (page >= 0 && pos0 + p < p_end) {
+                    const uint32_t* r = reinterpret_cast<const uint32_t*>(
+                        a.pool + t5k_offset(a.num_layers, a.num_kv_heads, page, a.layer, g, 0, pos0 % kPageSize + p));
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) w[m] = __ldg(r + 16 * hh + m);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) w[16 + m] = __ldg(r + 32 + 4 * hh + m);
+                    w[20] = __ldg(r + 40);
+                } else {
+#pragma unroll
+                    for (int m = 0; m < 21; ++m) w[m] = 0u;
+                }
+            };
+            uint32_t wn[21];
+            fetch_half(0, 0, wn);
+            bool ok = true;
+            for (int i = 0; i < n_tiles; ++i) {
+                const bool valid = ok && p_begin + i * kTileP + p < p_end;
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t w[21];
+#pragma unroll
+                    for (int m = 0; m < 21; ++m) w[m] = wn[m];
+                    fetch_half(hh ? i + 1 : i, hh ^ 1, wn);
+                    if (i > 0) ok = ok && warp_wait(&bar.qk_done[hh], (uint32_t)((i - 1) & 1), abort);
+                    tc_fence_after();
+                    const float s = __half2float(__ushort_as_half((unsigned short)(hh ? (w[20] >> 16) : (w[20] & 0xFFFFu))));
+                    range_bad |= valid && !(s <= kMaxT5kScale);
+                    const uint32_t col = tmem + lane_base + 64 * hh;
+#pragma unroll
+                    for (int bb = 0; bb < 4; ++bb) {
+                        uint32_t hi[16], lo[16];
+                        const uint32_t top = w[16 + bb];
+#pragma unroll
+                        for (int m = 0; m < 16; ++m) {
+                            const uint32_t nw = w[4 * bb + m / 4];
+                            const int sh = 8 * (m % 4);
+                            const uint32_t c0 = ((nw >> sh) & 0xFu) | (((top >> (2 * m)) & 1u) << 4);
+                            const uint32_t c1 = ((nw >> (sh + 4)) & 0xFu) | (((top >> (2 * m + 1)) & 1u) << 4);
+                            const float v0 = __shfl_sync(0xffffffffu, cent, (int)c0) * s;
+                            const float v1 = __shfl_sync(0xffffffffu, cent, (int)c1) * s;
+                            const __half2 h2 = __floats2half2_rn(v0, v1);
+                            const float2 hf = __half22float2(h2);
+                            hi[m] = as_u32(h2);
+                            lo[m] = as_u32(__floats2half2_rn(v0 - hf.x, v1 - hf.y));
+                        }
+                        tmem_st16(col + kColKHi + 16 * bb, hi);
+                        tmem_st16(col + kColKLo + 16 * bb, lo);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar.kready[hh]);
+                }
+            }
         } else {
             // thread p's 112-byte record straight from the pool into registers,
             // a tile ahead (7 x 16-byte read-only loads)
@@ -1038,7 +1107,7 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                             make_uint4(h16[4 * c], h16[4 * c + 1], h16[4 * c + 2], h16[4 * c + 3]);
                 }
 #pragma unroll 1
-                for (int j = 0; j < 4 && FMT == kFmtQ3; ++j) {
+                for (int j = 0; j < 4 && FMT != kFmtFp8; ++j) {
                     __half* vl = sm.v[b][Fmt<FMT>::kLo ? 1 : 0];
 
                     const int pl = 8 * (j >> 1) + (lane & 7);
@@ -1070,7 +1139,7 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                 if (producer) {
                     mbar_arrive(&bar.v_ready[b]);
                     if (ok && i + 1 < n_tiles && !*abort) {
-                        issue_rec_copy<kRecB>(a, pt_row, g, 1, pos0 + kTileP, r0, kSubP, sm.vrec + kRecB * r0,
+                        issue_rec_copy<FMT>(a, pt_row, g, 1, pos0 + kTileP, r0, kSubP, sm.vrec + kRecB * r0,
                                               &bar.vfull[q][e]);
                         pend[e] = i + 1;
                     }
@@ -1222,7 +1291,7 @@ cudaError_t launch_verify_mma(const VerifyArgs& a, cudaStream_t stream) {
     // the shared-memory opt-in is a per-device function attribute: one flag per
     // (device, instantiation)
     constexpr int kMaxDevices = 64;
-    static std::atomic<bool> flags[kMaxDevices][4];
+    static std::atomic<bool> flags[kMaxDevices][6];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::atomic<bool>* attr_set = flags[dev];
@@ -1230,6 +1299,9 @@ cudaError_t launch_verify_mma(const VerifyArgs& a, cudaStream_t stream) {
     if (a.fmt == kFmtFp8)
         return f32 ? launch_typed<float, kFmtFp8>(a, stream, attr_set[2])
                    : launch_typed<__nv_bfloat16, kFmtFp8>(a, stream, attr_set[3]);
+    if (a.fmt == kFmtT5k)
+        return f32 ? launch_typed<float, kFmtT5k>(a, stream, attr_set[4])
+                   : launch_typed<__nv_bfloat16, kFmtT5k>(a, stream, attr_set[5]);
     return f32 ? launch_typed<float, kFmtQ3>(a, stream, attr_set[0])
                : launch_typed<__nv_bfloat16, kFmtQ3>(a, stream, attr_set[1]);
 }

@@ -193,10 +193,11 @@ def test_prefill_and_t5k_host_checks(lib):
     n = ctypes.c_size_t()
     assert lib.q3kv_t5k_pool_bytes(ctypes.byref(d), ctypes.byref(n)) == 0
     assert n.value == 40 * 2 * 2 * 256 * (164 + 112)
-    # the turbo5k cache is read by the CUDA-core leg only
+    # the turbo5k cache is read by both legs: with null buffers the tensor-core leg's call gets
+    # past the plan and stops at the pointer checks instead of being refused
     args = [None, ctypes.byref(d), None, None, 4, None, None, None, 1, 1000, 4, 0, None, 0, None,
             _lib.Q3KV_IMPL_MMA, 256, None, 0, None]
-    assert lib.q3kv_t5k_verify_attn(*args) == _lib.Q3KV_ERR_UNSUPPORTED
+    assert lib.q3kv_t5k_verify_attn(*args) == _lib.Q3KV_ERR_INVALID_ARG
     assert lib.q3kv_t5k_append(None, ctypes.byref(d), None, None, 4, None, None, None, 1, 1, 5, None, None, 0,
                                None) == _lib.Q3KV_ERR_INVALID_ARG        # a layer outside the pool
 

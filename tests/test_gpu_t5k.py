@@ -2,8 +2,9 @@
 
 K records (5-bit Lloyd-Max codes, nibble and 5th-bit planes, two fp16 scales)
 and V records (the 3-bit codec) bit-exact against ``oracle.turbo5k``; verify
-outputs of the CUDA-core leg within max-abs 2e-3 / relative L2 1e-3 of the
-float64 attention over the decoded values.
+outputs of both legs within max-abs 2e-3 / relative L2 1e-3 of the float64
+attention over the decoded values (the tensor-core leg reads K_hat rounded to
+float32 and split into fp16 hi/lo).
 """
 import numpy as np
 import pytest
@@ -55,7 +56,7 @@ class T5kCache:
         offs = np.concatenate([[0], np.cumsum(n_q)]).astype(np.int32)
         q = torch.from_numpy(np.concatenate(q_rows)).to(tdtype(w)).cuda()
         out = torch.full((q.shape[0], w.num_q_heads, 256), float("nan"), dtype=torch.float32, device="cuda")
-        nbytes = self.api.workspace_bytes(self.desc, w.num_slots, max(ctx_len), max(n_q), 1, split_positions)
+        nbytes = self.api.workspace_bytes(self.desc, w.num_slots, max(ctx_len), max(n_q), impl, split_positions)
         ws = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device="cuda")
         self.api.t5k_verify_attn(self.desc, self.pool, self.page_table, torch.tensor(np.asarray(ctx_len, np.int32)).cuda(),
                                  torch.tensor(np.asarray(n_q, np.int32)).cuda(), torch.from_numpy(offs).cuda(),
@@ -84,8 +85,9 @@ def _small(dtype, dist, slots):
     return qi.Workload(base.key, "small", 19, slots, 2, (0, 0), (0, 0), 1, dtype, dist, dist)
 
 
+@pytest.mark.parametrize("impl", [1, 2])
 @pytest.mark.parametrize("dtype,dist", [("f32", "outlier8"), ("bf16", "loguniform10")])
-def test_t5k_records_bit_exact_and_verify(dtype, dist):
+def test_t5k_records_bit_exact_and_verify(dtype, dist, impl):
     w = _small(dtype, dist, 1)
     N, T = 700, 6
     c = T5kCache(w, [N + T])
@@ -99,11 +101,12 @@ def test_t5k_records_bit_exact_and_verify(dtype, dist):
         assert np.array_equal(c.records(0, 0, g, 1, N + T), q3packing.pack_records(vc, vs))
     q = qi.q_rows(w, 0, 0, 0, T)
     for split in (256, 0):
-        check_close(c.verify(0, [N + T], [T], [q], split_positions=split), _oracle(w, N, q, k, v))
+        check_close(c.verify(0, [N + T], [T], [q], split_positions=split, impl=impl), _oracle(w, N, q, k, v))
     assert int(c.status.item()) == 0
 
 
-def test_t5k_ragged_slots():
+@pytest.mark.parametrize("impl", [1, 2])
+def test_t5k_ragged_slots(impl):
     w = _small("bf16", "outlier8", 3)
     ctx = [5, 300, 1500]
     T = [1, 8, 16]
@@ -113,16 +116,20 @@ def test_t5k_ragged_slots():
     c.append(1, ctx, [(k[ctx[b]:], v[ctx[b]:]) for b, (k, v) in enumerate(kvs)])
     qs = [qi.q_rows(w, b, 1, 0, T[b]) for b in range(3)]
     want = np.concatenate([_oracle(w, ctx[b], qs[b], *kvs[b]) for b in range(3)])
-    check_close(c.verify(1, [n + t_ for n, t_ in zip(ctx, T)], T, qs), want)
+    check_close(c.verify(1, [n + t_ for n, t_ in zip(ctx, T)], T, qs, impl=impl), want)
     assert int(c.status.item()) == 0
 
 
-def test_t5k_tensor_core_leg_is_unsupported():
-    from speculative_verify_attention_q3kv_gb300 import _lib
-    w = _small("f32", "outlier8", 1)
-    c = T5kCache(w, [260])
-    k, v = slot_kv(w, 0, 0, 0, 260)
-    c.append(0, [0], [(k, v)])
-    with pytest.raises(_lib.Q3KVError) as e:
-        c.verify(0, [260], [4], [qi.q_rows(w, 0, 0, 0, 4)], impl=2)
-    assert e.value.code == _lib.Q3KV_ERR_UNSUPPORTED
+def test_t5k_outlier_heavy_verify_shapes_tensor_core_leg():
+    """Verify widths 6..16 over 4K+ positions, queries and cache both with 10x channels."""
+    w = _small("bf16", "loguniform10", 2)
+    ctx, T = [4096, 5000], [6, 16]
+    L = [n + t_ for n, t_ in zip(ctx, T)]
+    c = T5kCache(w, L, num_layers=1)
+    kvs = [slot_kv(w, b, 0, 0, L[b]) for b in range(2)]
+    c.append(0, [0, 0], kvs)
+    qs = [qi.q_rows(w, b, 0, 0, T[b]) for b in range(2)]
+    want = np.concatenate([_oracle(w, ctx[b], qs[b], *kvs[b]) for b in range(2)])
+    for split in (0, 256):
+        check_close(c.verify(0, L, T, qs, split_positions=split, impl=2), want)
+    assert int(c.status.item()) == 0
