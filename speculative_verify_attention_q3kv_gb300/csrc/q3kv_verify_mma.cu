@@ -49,26 +49,31 @@
 // (cp.async.bulk completing on their own mbarrier) and refill them as soon as
 // they have read them.  A tile's 128 positions are contiguous in a page.
 //
-// Warp roles (16 warps), handing tiles on with mbarriers:
-//   A   warps 0-3   softmax: thread = position; reads S from TMEM;
-//                   scores are in log2 units and the running row maximum is
-//                   only raised when a score exceeds it by more than 8 (then l
-//                   and the O^T columns are rescaled), so most tiles need no
-//                   cross-lane maximum; P = 2^(s - m) <= 256 goes to shared
-//                   memory as fp16 hi/lo; row sums accumulate per lane in TMEM
-//                   and are reduced across lanes once, after the last tile.
-//   B1  warps 4-7   thread = position: its K record in registers, K_hat into
+// Warp roles (20 warps, 96 registers each), handing tiles on with mbarriers:
+//   A   warps 0-7   softmax: thread = position (lane quarter warp & 3) for 32
+//                   query rows (warp >> 2 picks rows 0-31 or 32-63); reads its
+//                   S columns from TMEM; scores are in log2 units and the
+//                   running row maximum is only raised when a score exceeds it
+//                   by more than 8 (then l and the O^T columns of those rows
+//                   are rescaled; each 32-row half decides on its own), so most
+//                   tiles need no cross-lane maximum; P = 2^(s - m) <= 256 goes
+//                   to shared memory as fp16 hi/lo; row sums accumulate per lane
+//                   in TMEM and are reduced across lanes once, after the last
+//                   tile.  Two warps per lane quarter halve each warp's chain
+//                   of dependent work per tile, which is what sets the tile rate
+//                   when every scheduler also runs dequantising warps.
+//   B1  warps 8-11  thread = position: its K record in registers, K_hat into
 //                   TMEM in two halves (dims 0..127, 128..255), each as soon
 //                   as the QK half of the previous tile has read it.
-//   B2  warps 8-11  V_hat in 16-position sub-tiles through a ring of five
+//   B2  warps 12-15 V_hat in 16-position sub-tiles through a ring of five
 //                   shared-memory buffers; warp q fills sub-tiles q and q + 4
 //                   of each tile, lane = (position, 32-dim block).
-//   MQa, MQb  warps 12-13   one thread each issues a QK half
-//   MP0, MP1  warps 14-15   one thread each issues the PV of an O^T half
+//   MQa, MQb  warps 16-17   one thread each issues a QK half
+//   MP0, MP1  warps 18-19   one thread each issues the PV of an O^T half
 // TMEM (512 columns): K_hat hi | K_hat lo | S | row-sum partials | O^T dims 0..127 | 128..255.
 //
-// After the last tile the A warps read O^T (thread = one output dim, 32 rows
-// per TMEM round trip) and either finish the rows (one split: times 1/l, then
+// After the last tile the A warps read O^T (thread = one output dim, warp >> 2
+// picks the 128-dim half, 16 rows per TMEM round trip) and either finish the rows (one split: times 1/l, then
 // H back for the rotated format) or store the split partial (m, l, o) for the
 // merge kernel.
 //
@@ -89,7 +94,7 @@
 namespace q3kv {
 namespace {
 
-constexpr int kWarps = 16;
+constexpr int kWarps = 20;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTileP = 128;                 // positions per tile (MMA M of S^T)
 constexpr int kSubP = 16;                   // positions per V sub-tile (one MMA K step)
@@ -132,15 +137,16 @@ constexpr uint32_t kColO1 = 448;
 constexpr uint32_t kTmemCols = 512;
 
 // named barriers
-constexpr int kBarA = 1;                    // the 128 softmax threads
+constexpr int kBarA = 1;                    // the 256 softmax threads
+constexpr int kBarHalf = 2;                 // + h: the 128 softmax threads of rows 32h .. 32h + 31
 
 struct Bars {
     unsigned long long vfull[4][2]; // V records of B2 warp q's sub-tile q + 4e landed
     unsigned long long kready[2];   // K_hat dims half in TMEM (4 B1 warps)
     unsigned long long qk_done[2];  // QK half h done (S complete after half 1), that K_hat half read
-    unsigned long long s_free;      // S read (4 A warps)
+    unsigned long long s_free;      // S read (8 A warps)
     unsigned long long q_ready;     // Q hi/lo copied in (bulk copy bytes)
-    unsigned long long p_ready[2];  // P^T buffer b stored, O^T rescaled (4 A warps)
+    unsigned long long p_ready[2];  // P^T buffer b stored, O^T rescaled (8 A warps)
     unsigned long long v_ready[kVBufs];  // V_hat buffer b filled (one B2 warp)
     unsigned long long v_free[kVBufs];   // V_hat buffer b read (2 commits)
     unsigned long long pv_done[2];  // all PV MMAs of a tile with P^T buffer b done (2 commits)
@@ -414,7 +420,8 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& p01, uint32_
 // P_lo . V_hat_lo, are below 2^-20 of the scores and of P . V_hat (a 6-bit
 // s_hi left Q_lo . K_hat_lo at 2^-18, which at scores near 100 in log2 units,
 // with outlier-heavy queries and keys, alone cost up to 2e-3 of output).
-__device__ __forceinline__ void dequant_block(const uint32_t* w3, __half s, uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+template <int M0 = 0, int NM = 16>
+__device__ __forceinline__ void dequant_block(const uint32_t* w3, __half s, uint32_t (&hi)[NM], uint32_t (&lo)[NM]) {
     const __half s_hi = __ushort_as_half((unsigned short)(__half_as_ushort(s) & 0xFFF8u));
     const __half s_lo = __hsub(s, s_hi);
     const __half m12 = __ushort_as_half((unsigned short)0xCA00u);   // -12
@@ -425,7 +432,8 @@ __device__ __forceinline__ void dequant_block(const uint32_t* w3, __half s, uint
     const __half2 cl2 = __halves2half2(cl, cl);
     const uint32_t w0 = w3[0], w1 = w3[1], w2 = w3[2];
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
+    for (int mm = 0; mm < NM; ++mm) {
+        const int m = M0 + mm;                           // pair m of the block
         uint32_t x;
         if (m < 15) {
             const uint32_t w = (m < 5) ? w0 : (m < 10 ? w1 : w2);
@@ -433,8 +441,8 @@ __device__ __forceinline__ void dequant_block(const uint32_t* w3, __half s, uint
         } else {
             x = code_pair_last(w0, w1, w2);
         }
-        hi[m] = as_u32(__hfma2(as_h2(x), sh2, ch2));     // (c - 3.5) s_hi, exact
-        lo[m] = as_u32(__hfma2(as_h2(x), sl2, cl2));     // (c - 3.5) s_lo, exact
+        hi[mm] = as_u32(__hfma2(as_h2(x), sh2, ch2));    // (c - 3.5) s_hi, exact
+        lo[mm] = as_u32(__hfma2(as_h2(x), sl2, cl2));    // (c - 3.5) s_lo, exact
     }
 }
 
@@ -580,7 +588,7 @@ __global__ void __launch_bounds__(256) qprep_kernel(VerifyArgs a) {
 }
 
 template <typename TIn, int FMT>
-__global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) verify_mma_kernel(VerifyArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     MmaSmem<FMT>& sm = *reinterpret_cast<MmaSmem<FMT>*>(smem_raw);
     constexpr int kRecB = Fmt<FMT>::kRecB;
@@ -644,10 +652,10 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         for (int h = 0; h < 2; ++h) {
             mbar_init(&bar.kready[h], 4);
             mbar_init(&bar.qk_done[h], 1);
-            mbar_init(&bar.p_ready[h], 4);
+            mbar_init(&bar.p_ready[h], 8);
             mbar_init(&bar.pv_done[h], 2);
         }
-        mbar_init(&bar.s_free, 4);
+        mbar_init(&bar.s_free, 8);
         mbar_init(&bar.q_ready, 1);
         for (int b = 0; b < kVBufs; ++b) {
             mbar_init(&bar.v_ready[b], 1);
@@ -657,7 +665,7 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         sm.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 12) tmem_alloc(&sm.tmem_base, kTmemCols);
+    if (warp == 16) tmem_alloc(&sm.tmem_base, kTmemCols);
     if (tid < kRows) {
         // padding rows (>= Rc) get a running maximum of 0 and a threshold no
         // score exceeds: they never trigger a rescale and are never stored
@@ -668,7 +676,7 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp >= 8 && warp < 12 && lane == 0 && n_tiles > 0) {
+    if (warp >= 12 && warp < 16 && lane == 0 && n_tiles > 0) {
         // each V-dequantising warp copies its own positions of the first tile
         const int q = warp & 3;
         for (int e = 0; e < 2; ++e) {
@@ -676,7 +684,7 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
             issue_rec_copy<FMT>(a, pt_row, g, 1, p_begin, r0, kSubP, sm.vrec + kRecB * r0, &bar.vfull[q][e]);
         }
     }
-    if (warp == 12 && lane == 0) {
+    if (warp == 16 && lane == 0) {
         // the rotated queries of this unit, written by the query kernel that
         // precedes this grid: wait for it, then one bulk copy of hi and lo
         asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -689,11 +697,14 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
     bool range_bad = false;
     float* outs = reinterpret_cast<float*>(sm.qhi);      // [64][256] floats once Q is no longer read
 
-    if (warp < 4) {
+    if (warp < 8) {
         // ================================================================ A: softmax
-        const int q = warp;
+        const int q = warp & 3;                         // lane quarter: positions 32q .. 32q + 31
+        const int rh = warp >> 2;                       // rows 32rh .. 32rh + 31 (S^T columns)
+        const int r0 = 32 * rh;
         const int p = 32 * q + lane;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const int bar_half = kBarHalf + rh;
         bool ok = true;
         for (int i = 0; i < n_tiles; ++i) {
             const int pb = i & 1;                       // P^T buffer of this tile
@@ -701,18 +712,18 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
             // so its commit covers the whole S
             ok = ok && mbar_wait(&bar.qk_done[1], (uint32_t)(i & 1), abort);
             tc_fence_after();
-            // S, in one TMEM round trip; columns >= N are -inf
-            float x[kRows];
+            // this warp's 32 S columns, in one TMEM round trip; columns >= N are -inf
+            float x[32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                if (16 * c < N) tmem_ld16(tmem + lane_base + kColS + 16 * c, &x[16 * c]);
+            for (int c = 0; c < 2; ++c)
+                if (r0 + 16 * c < N) tmem_ld16(tmem + lane_base + kColS + r0 + 16 * c, &x[16 * c]);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.s_free);
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                if (16 * c >= N)
+            for (int c = 0; c < 2; ++c)
+                if (r0 + 16 * c >= N)
 #pragma unroll
                     for (int k = 0; k < 16; ++k) x[16 * c + k] = -CUDART_INF_F;
 
@@ -726,43 +737,42 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                 // rows r >= 8 (pos - Nctx) - row0; nothing past p_end is seen.
                 const int r_min = (tile_ok && pos < p_end) ? max(0, kGroup * (pos - Nctx) - row0) : kRows;
 #pragma unroll
-                for (int j = 0; j < kRows; ++j)
-                    if (j < r_min) x[j] = -CUDART_INF_F;
+                for (int j = 0; j < 32; ++j)
+                    if (r0 + j < r_min) x[j] = -CUDART_INF_F;
             }
             int over = 0;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const float4 t4 = reinterpret_cast<const float4*>(sm.thr)[c];
+            for (int c = 0; c < 8; ++c) {
+                const float4 t4 = reinterpret_cast<const float4*>(sm.thr + r0)[c];
                 over |= (x[4 * c] > t4.x) | (x[4 * c + 1] > t4.y) | (x[4 * c + 2] > t4.z) | (x[4 * c + 3] > t4.w);
             }
-            const int slow = named_or(kBarA, 128, over);
+            const int slow = named_or(bar_half, 128, over);
             if (slow) {
-                // raise the running maxima to cover this tile; rescale l (O below)
-#pragma unroll 1
-                for (int c = 0; c < 2; ++c) {
-                    if (32 * c < N) {
-                        float t[32];
+                // raise the running maxima of these 32 rows to cover this tile;
+                // rescale their l and O^T columns below
+                {
+                    float t[32];
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) t[k] = c ? x[32 + k] : x[k];
-                        sm.red[q][32 * c + lane] = transpose_reduce<true>(t);
-                    }
+                    for (int k = 0; k < 32; ++k) t[k] = x[k];
+                    sm.red[q][r0 + lane] = transpose_reduce<true>(t);
                 }
-                named_sync(kBarA, 128);
-                if (tid < Rc) {
-                    const float mt = fmaxf(fmaxf(sm.red[0][tid], sm.red[1][tid]), fmaxf(sm.red[2][tid], sm.red[3][tid]));
-                    const float m_old = sm.m_run[tid];
+                named_sync(bar_half, 128);
+                if (q == 0 && r0 + lane < Rc) {
+                    const int r = r0 + lane;
+                    const float mt = fmaxf(fmaxf(sm.red[0][r], sm.red[1][r]), fmaxf(sm.red[2][r], sm.red[3][r]));
+                    const float m_old = sm.m_run[r];
                     const float m_new = fmaxf(m_old, mt);
                     const float al = exp2f(m_old - m_new);
-                    sm.m_run[tid] = m_new;
-                    sm.thr[tid] = m_new + kRescaleThreshold;
-                    sm.alpha[tid] = al;
+                    sm.m_run[r] = m_new;
+                    sm.thr[r] = m_new + kRescaleThreshold;
+                    sm.alpha[r] = al;
                 }
-                named_sync(kBarA, 128);
+                named_sync(bar_half, 128);
             }
             // P = 2^(s - m) in place (a masked score gives 0)
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const float4 m4 = reinterpret_cast<const float4*>(sm.m_run)[c];
+            for (int c = 0; c < 8; ++c) {
+                const float4 m4 = reinterpret_cast<const float4*>(sm.m_run + r0)[c];
                 x[4 * c] = fast_exp2(x[4 * c] - m4.x);
                 x[4 * c + 1] = fast_exp2(x[4 * c + 1] - m4.y);
                 x[4 * c + 2] = fast_exp2(x[4 * c + 2] - m4.z);
@@ -773,11 +783,12 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
             if (slow && i > 0) {
                 ok = ok && mbar_wait(&bar.pv_done[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1), abort);
                 tc_fence_after();
+                const int c_end = min(r0 + 32, N);
 #pragma unroll 1
                 for (int h = 0; h < 3; ++h) {           // O^T halves and the row-sum partials
                     const uint32_t col = h == 0 ? kColO0 : (h == 1 ? kColO1 : kColL);
 #pragma unroll 1
-                    for (int c = 0; c < N; c += 8) {
+                    for (int c = r0; c < c_end; c += 8) {
                         float v8[8];
                         tmem_ld8(tmem + lane_base + col + c, v8);
                         tmem_ld_wait();
@@ -794,8 +805,8 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
             __half* phi = sm.phi[pb];
             __half* plo = sm.plo[pb];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                if (8 * c < N) {
+            for (int c = 0; c < 4; ++c) {
+                if (r0 + 8 * c < N) {
                     uint32_t h4[4], l4[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -805,8 +816,8 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                         h4[k] = as_u32(hh2);
                         l4[k] = as_u32(__floats2half2_rn(a0 - hf.x, a1 - hf.y));
                     }
-                    *reinterpret_cast<uint4*>(&phi[p_off(8 * c, p)]) = make_uint4(h4[0], h4[1], h4[2], h4[3]);
-                    *reinterpret_cast<uint4*>(&plo[p_off(8 * c, p)]) = make_uint4(l4[0], l4[1], l4[2], l4[3]);
+                    *reinterpret_cast<uint4*>(&phi[p_off(r0 + 8 * c, p)]) = make_uint4(h4[0], h4[1], h4[2], h4[3]);
+                    *reinterpret_cast<uint4*>(&plo[p_off(r0 + 8 * c, p)]) = make_uint4(l4[0], l4[1], l4[2], l4[3]);
                 }
             }
             fence_proxy_async();
@@ -816,12 +827,12 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
             // row sums: this thread's P values added to its lane's TMEM partials
             // (the cross-lane sum is taken once, after the last tile)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (16 * c < N) {
+            for (int c = 0; c < 2; ++c) {
+                if (r0 + 16 * c < N) {
                     uint32_t u16[16];
                     if (i > 0) {
                         float y[16];
-                        tmem_ld16(tmem + lane_base + kColL + 16 * c, y);
+                        tmem_ld16(tmem + lane_base + kColL + r0 + 16 * c, y);
                         tmem_ld_wait();
 #pragma unroll
                         for (int k = 0; k < 16; ++k) u16[k] = __float_as_uint(y[k] + x[16 * c + k]);
@@ -829,35 +840,31 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
 #pragma unroll
                         for (int k = 0; k < 16; ++k) u16[k] = __float_as_uint(x[16 * c + k]);
                     }
-                    tmem_st16(tmem + lane_base + kColL + 16 * c, u16);
+                    tmem_st16(tmem + lane_base + kColL + r0 + 16 * c, u16);
                 }
             }
             tmem_st_wait();
         }
         // l = column sums of the row-sum partials over the 128 lanes
         {
-            float y[kRows];
+            float y[32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (16 * c < N) tmem_ld16(tmem + lane_base + kColL + 16 * c, &y[16 * c]);
+            for (int c = 0; c < 2; ++c) {
+                if (r0 + 16 * c < N && n_tiles > 0) tmem_ld16(tmem + lane_base + kColL + r0 + 16 * c, &y[16 * c]);
                 else
 #pragma unroll
                     for (int k = 0; k < 16; ++k) y[16 * c + k] = 0.0f;
             }
             tmem_ld_wait();
-            if (n_tiles == 0)
-#pragma unroll
-                for (int k = 0; k < kRows; ++k) y[k] = 0.0f;
-            sm.red[q][lane] = transpose_reduce<false>(*reinterpret_cast<float(*)[32]>(&y[0]));
-            if (N > 32) sm.red[q][32 + lane] = transpose_reduce<false>(*reinterpret_cast<float(*)[32]>(&y[32]));
-            named_sync(kBarA, 128);
+            sm.red[q][r0 + lane] = transpose_reduce<false>(y);
+            named_sync(kBarA, 256);
             if (tid < N) {
                 const float l = (sm.red[0][tid] + sm.red[1][tid]) + (sm.red[2][tid] + sm.red[3][tid]);
                 sm.l_run[tid] = l;
                 sm.alpha[tid] = (n_splits == 1) ? 1.0f / l : 1.0f;   // the epilogue's row multiplier
             }
         }
-        named_sync(kBarA, 128);   // l_run complete
+        named_sync(kBarA, 256);   // l_run complete
         // ---- epilogue: O^T -> partial or finished rows
         if (n_tiles > 0) ok = ok && mbar_wait(&bar.pv_done[(n_tiles - 1) & 1], (uint32_t)(((n_tiles - 1) >> 1) & 1), abort);
         tc_fence_after();
@@ -867,19 +874,16 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
             // 16 rows of this thread's dim per TMEM round trip: a short loop,
             // since this code runs once per CTA and is fetched cold
             float* dst = (n_splits == 1) ? outs : po;
+            const int d = 128 * rh + 32 * q + lane;
+            const uint32_t col = rh ? kColO1 : kColO0;
 #pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                const int d = 128 * h + 32 * q + lane;
-                const uint32_t col = h ? kColO1 : kColO0;
-#pragma unroll 1
-                for (int c = 0; c < Rc; c += 16) {
-                    float v[16];
-                    tmem_ld16(tmem + lane_base + col + c, v);
-                    tmem_ld_wait();
+            for (int c = 0; c < Rc; c += 16) {
+                float v[16];
+                tmem_ld16(tmem + lane_base + col + c, v);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        if (c + k < Rc) dst[(c + k) * kHeadDim + d] = v[k] * sm.alpha[c + k];
-                }
+                for (int k = 0; k < 16; ++k)
+                    if (c + k < Rc) dst[(c + k) * kHeadDim + d] = v[k] * sm.alpha[c + k];
             }
             if (n_splits > 1 && tid < Rc) {
                 float* pml = a.part_ml + ((int64_t)unit * a.num_splits + split) * kRows * 2;
@@ -887,9 +891,9 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                 pml[2 * tid + 1] = sm.l_run[tid];
             }
         }
-    } else if (warp < 8) {
+    } else if (warp < 12) {
         // ================================================================ B1: K_hat -> TMEM
-        const int q = warp - 4;
+        const int q = warp - 8;
         const int p = 32 * q + lane;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         if constexpr (FMT == kFmtFp8) {
@@ -926,11 +930,11 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                     tc_fence_after();
                     const uint32_t col = tmem + lane_base + kColKHi + 64 * hh;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t h16[16];
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t h8[8];
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) e4m3x4_to_f16(w[8 * c + k], h16[2 * k], h16[2 * k + 1]);
-                        tmem_st16(col + 16 * c, h16);
+                        for (int k = 0; k < 4; ++k) e4m3x4_to_f16(w[4 * c + k], h8[2 * k], h8[2 * k + 1]);
+                        tmem_st8(col + 8 * c, h8);
                     }
                     tmem_st_wait();
                     tc_fence_before();
@@ -978,11 +982,13 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                     range_bad |= valid && !(s <= kMaxT5kScale);
                     const uint32_t col = tmem + lane_base + 64 * hh;
 #pragma unroll
-                    for (int bb = 0; bb < 4; ++bb) {
-                        uint32_t hi[16], lo[16];
+                    for (int e = 0; e < 8; ++e) {               // 8 pairs (16 dims) at a time
+                        const int bb = e >> 1;
+                        uint32_t hi[8], lo[8];
                         const uint32_t top = w[16 + bb];
 #pragma unroll
-                        for (int m = 0; m < 16; ++m) {
+                        for (int mm = 0; mm < 8; ++mm) {
+                            const int m = 8 * (e & 1) + mm;
                             const uint32_t nw = w[4 * bb + m / 4];
                             const int sh = 8 * (m % 4);
                             const uint32_t c0 = ((nw >> sh) & 0xFu) | (((top >> (2 * m)) & 1u) << 4);
@@ -991,11 +997,11 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                             const float v1 = __shfl_sync(0xffffffffu, cent, (int)c1) * s;
                             const __half2 h2 = __floats2half2_rn(v0, v1);
                             const float2 hf = __half22float2(h2);
-                            hi[m] = as_u32(h2);
-                            lo[m] = as_u32(__floats2half2_rn(v0 - hf.x, v1 - hf.y));
+                            hi[mm] = as_u32(h2);
+                            lo[mm] = as_u32(__floats2half2_rn(v0 - hf.x, v1 - hf.y));
                         }
-                        tmem_st16(col + kColKHi + 16 * bb, hi);
-                        tmem_st16(col + kColKLo + 16 * bb, lo);
+                        tmem_st8(col + kColKHi + 8 * e, hi);
+                        tmem_st8(col + kColKLo + 8 * e, lo);
                     }
                     tmem_st_wait();
                     tc_fence_before();
@@ -1049,12 +1055,22 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                     const uint32_t col = tmem + lane_base + 64 * hh;
 #pragma unroll
                     for (int bb = 0; bb < 4; ++bb) {
-                        uint32_t hi[16], lo[16];
+                        // eight pairs at a time keep the dequantised values in
+                        // 16 registers beside the two records
                         const __half s = __ushort_as_half((unsigned short)((bb & 1) ? (sh[bb >> 1] >> 16) : (sh[bb >> 1] & 0xFFFFu)));
-                        dequant_block(&wh[3 * bb], s, hi, lo);
                         range_bad |= valid && !(__half2float(s) <= kMaxScale);
-                        tmem_st16(col + kColKHi + 16 * bb, hi);
-                        tmem_st16(col + kColKLo + 16 * bb, lo);
+                        {
+                            uint32_t hi[8], lo[8];
+                            dequant_block<0, 8>(&wh[3 * bb], s, hi, lo);
+                            tmem_st8(col + kColKHi + 16 * bb, hi);
+                            tmem_st8(col + kColKLo + 16 * bb, lo);
+                        }
+                        {
+                            uint32_t hi[8], lo[8];
+                            dequant_block<8, 8>(&wh[3 * bb], s, hi, lo);
+                            tmem_st8(col + kColKHi + 16 * bb + 8, hi);
+                            tmem_st8(col + kColKLo + 16 * bb + 8, lo);
+                        }
                     }
                     tmem_st_wait();
                     tc_fence_before();
@@ -1063,12 +1079,12 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
                 }
             }
         }
-    } else if (warp < 12) {
+    } else if (warp < 16) {
         // ================================================================ B2: V_hat sub-tiles -> shared memory
         // Warp q fills sub-tiles q and q + 4 of every tile (sub-tile u = 8 i + s
         // goes to ring buffer u % 5) from its own two 16-record copies.  Lane = (position pl, 32-dim block
         // blk); item j covers pl = 8 (j >> 1) + (lane & 7), blk = 4 (j & 1) + (lane >> 3).
-        const int q = warp - 8;
+        const int q = warp - 12;
         const bool producer = (lane == 0);
         int pend[2] = {n_tiles > 0 ? 0 : -1, n_tiles > 0 ? 0 : -1};
         bool ok = true;
@@ -1149,9 +1165,9 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         if (producer)
             for (int e = 0; e < 2; ++e)
                 if (pend[e] >= 0) mbar_drain(&bar.vfull[q][e], (uint32_t)(pend[e] & 1));
-    } else if (warp < 14) {
+    } else if (warp < 18) {
         // ================================================================ MQa / MQb: QK halves
-        const int h = warp - 12;                     // 0: dims 0..127, 1: dims 128..255 (both into S)
+        const int h = warp - 16;                     // 0: dims 0..127, 1: dims 128..255 (both into S)
         const uint32_t idesc_qk = make_idesc(N, false, false);
         const uint64_t bq_hi = make_desc(smem_u32(sm.qhi) + h * 8 * 256, kQLbo, kQSbo);
         const uint64_t bq_lo = make_desc(smem_u32(sm.qlo) + h * 8 * 256, kQLbo, kQSbo);
@@ -1187,7 +1203,7 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
         if (h == 0 && !qok && lane == 0) mbar_drain(&bar.q_ready, 0);   // the Q copy, after a timeout
     } else {
         // ================================================================ MP0 / MP1: PV halves
-        const int h = warp - 14;                     // O^T dims 128h .. 128h + 127
+        const int h = warp - 18;                     // O^T dims 128h .. 128h + 127
         const uint32_t idesc_pv = make_idesc(N, true, true);
         const uint32_t dO = tmem + (h ? kColO1 : kColO0);
         const uint64_t bp_hi0 = make_desc(smem_u32(sm.phi[0]), kPLbo, kPSbo);
@@ -1234,7 +1250,7 @@ __global__ void __maxnreg__(128) verify_mma_kernel(VerifyArgs a) {
     if (range_bad && a.status) atomicOr(a.status, Q3KV_STATUS_RANGE);
     tc_fence_before();
     __syncthreads();
-    if (warp == 12) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 16) tmem_dealloc(tmem, kTmemCols);
     if (*abort) {
         if (tid == 0 && a.status) atomicOr(a.status, Q3KV_STATUS_TIMEOUT);
         return;
