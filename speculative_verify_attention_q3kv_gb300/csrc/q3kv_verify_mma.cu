@@ -54,9 +54,9 @@
 //                   query rows (warp >> 2 picks rows 0-31 or 32-63); reads its
 //                   S columns from TMEM; scores are in log2 units and the
 //                   running row maximum is only raised when a score exceeds it
-//                   by more than 8 (then l and the O^T columns of those rows
+//                   by more than 14 (then l and the O^T columns of those rows
 //                   are rescaled; each 32-row half decides on its own), so most
-//                   tiles need no cross-lane maximum; P = 2^(s - m) <= 256 goes
+//                   tiles need no cross-lane maximum; P = 2^(s - m) <= 2^14 goes
 //                   to shared memory as fp16 hi/lo; row sums accumulate per lane
 //                   in TMEM and are reduced across lanes once, after the last
 //                   tile.  Two warps per lane quarter halve each warp's chain
@@ -116,7 +116,7 @@ struct Fmt<kFmtFp8> {
     static constexpr bool kRot = false;
 };
 constexpr int kRows = 64;                   // max query rows per CTA (MMA N <= 64)
-constexpr float kRescaleThreshold = 8.0f;   // log2 units: P <= 256
+constexpr float kRescaleThreshold = 14.0f;  // log2 units: P <= 2^14, exact to split into fp16 hi/lo
 // Initial running maximum: finite, so 2^(s - m) of a masked score (-inf) is 0
 // without a select, and any finite score exceeds it by more than the threshold.
 constexpr float kMInit = -1.0e30f;
