@@ -82,10 +82,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_fma_kernel(VerifyArgs a) {
     const int lane = tid & 31;
     const int warp = tid >> 5;
 
-    // units run fastest in the grid (see the tensor-core leg)
+    // units run fastest in the grid, each slot's last row chunk first (see
+    // the tensor-core leg)
     const int unit_id = blockIdx.x;
     const int split = blockIdx.y;
-    const int chunk = unit_id % a.row_chunks;
+    const int chunk = a.row_chunks - 1 - unit_id % a.row_chunks;
     const int g = (unit_id / a.row_chunks) % a.num_kv_heads;
     const int slot = unit_id / (a.row_chunks * a.num_kv_heads);
 

@@ -600,10 +600,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_mma_kernel(VerifyArgs a) {
     const int warp = tid >> 5;
 
     // units run fastest in the grid, so every unit's first splits are
-    // dispatched before any unit's later ones (most of which exit at once)
+    // dispatched before any unit's later ones (most of which exit at once).
+    // Within a (slot, kv head) the last row chunk comes first: in a causal
+    // prefill a chunk's visible context grows with its index, so the longest
+    // CTAs are dispatched first and the short ones fill the last wave.
     const int unit_id = blockIdx.x;
     const int split = blockIdx.y;
-    const int chunk = unit_id % a.row_chunks;
+    const int chunk = a.row_chunks - 1 - unit_id % a.row_chunks;
     const int g = (unit_id / a.row_chunks) % a.num_kv_heads;
     const int slot = unit_id / (a.row_chunks * a.num_kv_heads);
 
