@@ -44,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 # from ncu captures of the current kernel in this benchmark's launch configuration
 # (profiles/); the roofline's traffic is this times the launch's positions.
 # Workloads without a capture of the current kernel report null.
-NCU_TRAFFIC_BYTES_PER_POSITION = {5: 227.16, 4: 234.04, 3: 229.60, 2: 227.67}
+NCU_TRAFFIC_BYTES_PER_POSITION = {5: 226.56, 4: 231.38, 3: 228.90, 2: 227.56}
 L2_FLUSH_BYTES = 256 << 20
 
 
