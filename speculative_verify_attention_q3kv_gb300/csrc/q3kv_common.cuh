@@ -13,14 +13,37 @@ namespace q3kv {
 __device__ __forceinline__ float load_in(const float* p) { return *p; }
 __device__ __forceinline__ float load_in(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
-// In-place unnormalised H (entries +-1) on rows [0, nrows) of a [rows][256]
-// float array in shared memory (16-byte aligned); all threads of the block
+// Unnormalised H (entries +-1) on one 256-element row held by a warp: lane l
+// holds elements 8l .. 8l + 7, so strides 1, 2 and 4 pair elements within a
+// lane and strides 8 .. 128 pair lane l with lane l ^ (stride / 8) (the lower
+// lane keeps a + b, the upper a - b).  The stages run in the radix-2 order,
+// stride 1 first, with the same two operations per pair, so the result equals
+// the element-by-element butterfly bit for bit.
+__device__ __forceinline__ void rotate_row_regs(float (&y)[8]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if ((i & h) == 0) {
+                const float a = y[i], b = y[i + h];
+                y[i] = a + b;
+                y[i + h] = a - b;
+            }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float o = __shfl_xor_sync(0xffffffffu, y[i], m);
+            y[i] = upper ? o - y[i] : y[i] + o;
+        }
+    }
+}
+
+// In-place unnormalised H on rows [0, nrows) of a [rows][256] float array in
+// shared memory (16-byte aligned), one warp per row; all threads of the block
 // take part (a block of whole warps), and the block is synchronised on return.
-// One warp per row: lane l holds elements 8l .. 8l + 7, so strides 1, 2 and 4
-// pair elements within a lane and strides 8 .. 128 pair lane l with lane
-// l ^ (stride / 8) (the lower lane keeps a + b, the upper a - b).  The stages
-// run in the radix-2 order, stride 1 first, with the same two operations per
-// pair, so the result equals the element-by-element butterfly bit for bit.
 __device__ inline void rotate_rows(float* x, int nrows) {
     const int lane = threadIdx.x & 31;
     const int nwarps = blockDim.x >> 5;
@@ -28,24 +51,7 @@ __device__ inline void rotate_rows(float* x, int nrows) {
         float4* row = reinterpret_cast<float4*>(x + r * kHeadDim + 8 * lane);
         const float4 u = row[0], w = row[1];
         float y[8] = {u.x, u.y, u.z, u.w, w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int h = 1; h < 8; h <<= 1)
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if ((i & h) == 0) {
-                    const float a = y[i], b = y[i + h];
-                    y[i] = a + b;
-                    y[i + h] = a - b;
-                }
-#pragma unroll
-        for (int m = 1; m < 32; m <<= 1) {
-            const bool upper = (lane & m) != 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float o = __shfl_xor_sync(0xffffffffu, y[i], m);
-                y[i] = upper ? o - y[i] : y[i] + o;
-            }
-        }
+        rotate_row_regs(y);
         row[0] = make_float4(y[0], y[1], y[2], y[3]);
         row[1] = make_float4(y[4], y[5], y[6], y[7]);
     }

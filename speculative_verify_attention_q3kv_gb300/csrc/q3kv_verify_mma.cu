@@ -1259,12 +1259,19 @@ __global__ void __launch_bounds__(kThreads, 1) verify_mma_kernel(VerifyArgs a) {
         return;
     }
     if (n_splits == 1) {
-        if (Fmt<FMT>::kRot) rotate_rows(outs, Rc);
+        // whole rows: H back (rotated format) and 1/16, one warp per row, from
+        // registers straight to the output
         constexpr float kOutScale = Fmt<FMT>::kRot ? 0.0625f : 1.0f;   // unnormalised H: 1/16
-        for (int idx = tid; idx < Rc * kHeadDim; idx += kThreads) {
-            const int r = idx / kHeadDim, dd = idx % kHeadDim;
+        for (int r = warp; r < Rc; r += kWarps) {
+            const float4* src = reinterpret_cast<const float4*>(outs + r * kHeadDim + 8 * lane);
+            const float4 u0 = src[0], u1 = src[1];
+            float y[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            if (Fmt<FMT>::kRot) rotate_row_regs(y);
             const int ra = row0 + r;
-            a.out[((q_base + ra / kGroup) * Hq + g * kGroup + ra % kGroup) * kHeadDim + dd] = outs[idx] * kOutScale;
+            float4* o4 = reinterpret_cast<float4*>(a.out + ((q_base + ra / kGroup) * Hq + g * kGroup + ra % kGroup) * kHeadDim +
+                                                   8 * lane);
+            o4[0] = make_float4(y[0] * kOutScale, y[1] * kOutScale, y[2] * kOutScale, y[3] * kOutScale);
+            o4[1] = make_float4(y[4] * kOutScale, y[5] * kOutScale, y[6] * kOutScale, y[7] * kOutScale);
         }
     }
 }
