@@ -44,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 # from ncu captures of the current kernel in this benchmark's launch configuration
 # (profiles/); the roofline's traffic is this times the launch's positions.
 # Workloads without a capture of the current kernel report null.
-NCU_TRAFFIC_BYTES_PER_POSITION = {5: 226.56, 4: 231.38, 3: 228.90, 2: 227.56}
+NCU_TRAFFIC_BYTES_PER_POSITION = {5: 226.61, 4: 232.06, 3: 228.80, 2: 227.56}
 L2_FLUSH_BYTES = 256 << 20
 
 
