@@ -102,6 +102,38 @@ def test_outlier_heavy_queries_and_cache_verify_shapes(impl, split):
 
 
 @pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("split", [0, 256])
+def test_score_jump_around_the_lagged_maximum_threshold(impl, split):
+    """One late key whose score for query row (token 0, head 0) exceeds every earlier score by
+    delta log2 units, per slot delta from 4 to 20: around 14 the tensor-core leg either keeps
+    its running maximum (P up to 2^14 in the fp16 hi/lo split) or rescales; both must hold."""
+    _impl_or_skip(impl)
+    deltas = [4.0, 12.0, 13.5, 13.9, 14.1, 14.5, 16.0, 20.0]
+    S, N, T = len(deltas), 1000, 4
+    w = _small("f32", "outlier8", slots=S)
+    L = [N + T] * S
+    c = GpuCache(w, L, num_layers=1)
+    kvs, qs = [], []
+    log2e = 1.4426950408889634
+    for b, delta in enumerate(deltas):
+        k, v = slot_kv(w, b, 0, 0, N + T)
+        q = qi.q_rows(w, b, 0, 0, T)
+        p_star = N - 50                              # in the context's last tile
+        u = q[0, 0].astype(np.float64)
+        prev = float(np.max(k[:p_star, 0].astype(np.float64) @ u)) / 16.0 * log2e
+        scale = (prev + delta) * 16.0 / (log2e * float(u @ u))
+        k = k.copy()
+        k[p_star, 0] = (scale * u).astype(np.float32)
+        kvs.append((k, v))
+        qs.append(q)
+    c.append_rows(0, list(range(S)), [0] * S, kvs)
+    want = np.concatenate([oracle_verify(w, b, 0, N, qs[b], *kvs[b]) for b in range(S)])
+    out = c.verify(0, L, [T] * S, qs, impl=impl, split_positions=split)
+    check_close(out, want)
+    assert int(c.status.item()) == 0
+
+
+@pytest.mark.parametrize("impl", IMPLS)
 def test_batched_equals_solo_bitwise(impl):
     _impl_or_skip(impl)
     w = _small("bf16", "loguniform10", slots=3)
