@@ -175,26 +175,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(VerifyArgs a, int 
         }
         x[4 * h] = t.x; x[4 * h + 1] = t.y; x[4 * h + 2] = t.z; x[4 * h + 3] = t.w;
     }
-    if (ROT) {
-#pragma unroll
-        for (int h = 1; h < 8; h <<= 1)
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if ((i & h) == 0) {
-                    const float lo = x[i], hi = x[i + h];
-                    x[i] = lo + hi;
-                    x[i + h] = lo - hi;
-                }
-#pragma unroll
-        for (int m = 1; m < 32; m <<= 1) {
-            const bool upper = (lane & m) != 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
-                x[i] = upper ? o - x[i] : x[i] + o;
-            }
-        }
-    }
+    if (ROT) rotate_row_regs(x);
     const int ra = row0 + r;
     const int Hq = a.num_kv_heads * kGroup;
     float* dst = a.out + (((int64_t)a.q_offsets[slot] + ra / kGroup) * Hq + g * kGroup + ra % kGroup) * kHeadDim + 8 * lane;
